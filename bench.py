@@ -1,0 +1,390 @@
+"""Benchmark of the FP8 MLA KV hot path: one step = the KV writer on a padded
+8,192-row batch (a random quarter aimed at slot 0) into a 1,048,576-slot cache,
+then the sparse top-k decode of 256 query tokens (16 heads, d_qk 576, top-k
+2,048, every entry present) over that cache.
+
+Prints ONE JSON line (rank 0). ``value`` is decode query-tokens/s over whole
+steps (writer + decode), all ranks together; the line also carries the decode's
+gathered-KV GB/s, the writer's rows/s, the roofline of the dominant kernel
+(decode) against the measured HBM peak, the clocks seen during the timed region,
+an end-to-end figure through the public API with host buffers, and the CPU
+oracle timed on a bounded sample on the host cores.
+
+``--impl reference`` times the CPU oracle (the only reference this method has)
+on the same workload, a bounded sample per step.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from fp8_mla_kv_gb300 import workloads  # noqa: E402
+
+METRIC = "sparse-MLA decode query-tokens/s & gathered-KV HBM GB/s; KV-writer rows/s"
+UNIT = "query-tokens/s"
+WRITE_LABEL = "sweep.8192.pad"
+KERNEL_SRC = ["fp8_mla_kv_gb300/csrc/mla_sparse_decode.cu", "fp8_mla_kv_gb300/csrc/mla_device.cuh"]
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_sweep_traffic.txt")
+
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def kernel_sha() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SRC:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic():
+    """ncu DRAM bytes per decode launch, if recorded for the current kernel source."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    txt = open(TRAFFIC_FILE).read()
+    m_b = re.search(r"traffic_bytes_per_launch\s*=\s*(\d+)", txt)
+    m_s = re.search(r"kernel_source_sha\s*=\s*([0-9a-f]+)", txt)
+    if m_b and m_s and m_s.group(1) == kernel_sha():
+        return int(m_b.group(1))
+    return None
+
+
+class ClockSampler:
+    FIELDS = ["index", "clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.dev = device_index
+
+    def start(self):
+        cmd = ["nvidia-smi", "--query-gpu=" + ",".join(self.FIELDS), "--format=csv,noheader,nounits", "-lms", "100"]
+        try:
+            uuid = str(torch.cuda.get_device_properties(self.dev).uuid)
+            cmd += ["-i", uuid if uuid.startswith("GPU-") else "GPU-" + uuid]
+        except Exception:
+            pass
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.25)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out = ""
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < len(self.FIELDS):
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def oracle_cpu_baseline(wl, cache_np, wb, seconds: float = 12.0):
+    """Oracle decode (float64, all host cores) on a bounded sample of the tokens."""
+    import oracle
+    db = wl.decode
+    cores = oracle.default_threads()
+    topk = db.topk.numpy()
+    t0 = time.perf_counter()
+    oracle.sparse_decode(db.q, cache_np, topk, db.sm_scale, tokens=[0], n_threads=1)
+    one = max(time.perf_counter() - t0, 1e-3)          # single-thread seconds per token
+    n_tok = int(max(cores, min(db.T, seconds * cores / one)))
+    n_tok = min(n_tok, db.T)
+    toks = list(range(n_tok))
+    t0 = time.perf_counter()
+    oracle.sparse_decode(db.q, cache_np, topk, db.sm_scale, tokens=toks, n_threads=cores)
+    dt = time.perf_counter() - t0
+    return {"value": n_tok / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"float64 oracle decode of {n_tok} of the {db.T} query tokens "
+                      f"(H={db.H}, W={db.W}, all present) in {dt:.2f} s on {cores} threads"}
+
+
+def build_cache_gpu(wl, dev):
+    from fp8_mla_kv_gb300 import mlasparse as M
+    cache = torch.full((wl.num_slots, 656), wl.slot0_byte, dtype=torch.uint8, device=dev)
+    f = wl.fill
+    chunk = 1 << 18
+    for r0 in range(0, f.slot_idx.shape[0], chunk):
+        r1 = min(f.slot_idx.shape[0], r0 + chunk)
+        M.mla_kv_write(cache, f.slot_idx[r0:r1].to(dev), f.latent[r0:r1].to(dev),
+                       None if f.rope is None else f.rope[r0:r1].to(dev))
+    torch.cuda.synchronize()
+    return cache
+
+
+def run_ours(args, rank, world, local_rank):
+    from fp8_mla_kv_gb300 import build as B
+    from fp8_mla_kv_gb300 import mlasparse as M
+    B.build()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    wl = workloads.sweep()
+    wb = next(w for w in wl.writes if w.label == WRITE_LABEL)
+    db = wl.decode
+    cache = build_cache_gpu(wl, dev)
+
+    slots_d, lat_d, rope_d = wb.slot_idx.to(dev), wb.latent.to(dev), wb.rope.to(dev)
+    q_d, topk_d = db.q.to(dev), db.topk.to(dev)
+    out_d = torch.empty((db.T, db.H, 512), dtype=torch.bfloat16, device=dev)
+    lse_d = torch.empty((db.T, db.H), dtype=torch.float32, device=dev)
+    ws = M.alloc_workspace(db.T, db.H, db.W, dev)
+    launches_per_step = 1 + 1 + (1 if ws is not None else 0)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+
+    def step():
+        M.mla_kv_write(cache, slots_d, lat_d, rope_d)
+        M.mla_sparse_decode(q_d, cache, topk_d, db.sm_scale, out=out_d, lse=lse_d, workspace=ws)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    assert M.mla_get_error() == 0
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    sampler = ClockSampler(local_rank)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    wall0 = time.perf_counter()
+    for k in range(K):
+        flush.zero_()                      # L2 flushed between timed steps (not timed)
+        ev[k][0].record()
+        M.mla_kv_write(cache, slots_d, lat_d, rope_d)
+        ev[k][1].record()
+        M.mla_sparse_decode(q_d, cache, topk_d, db.sm_scale, out=out_d, lse=lse_d, workspace=ws)
+        ev[k][2].record()
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop()
+    w_ms = [ev[k][0].elapsed_time(ev[k][1]) for k in range(K)]
+    d_ms = [ev[k][1].elapsed_time(ev[k][2]) for k in range(K)]
+    s_ms = [ev[k][0].elapsed_time(ev[k][2]) for k in range(K)]
+    assert M.mla_get_error() == 0
+
+    # End to end through the public API with pinned host buffers: per step the
+    # inputs go host -> device, the outputs come back device -> host.
+    h_in = [t.pin_memory() for t in (wb.slot_idx, wb.latent, wb.rope, db.q, db.topk)]
+    h_out = torch.empty((db.T, db.H, 512), dtype=torch.bfloat16).pin_memory()
+    h_lse = torch.empty((db.T, db.H), dtype=torch.float32).pin_memory()
+    d_in = [torch.empty_like(t, device=dev) for t in h_in]
+    h2d = sum(t.numel() * t.element_size() for t in h_in)
+    d2h = h_out.numel() * 2 + h_lse.numel() * 4
+    e2e_steps = max(3, min(K, 200))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_ms = []
+    for k in range(e2e_steps + 2):
+        flush.zero_()
+        e0.record()
+        for d, h in zip(d_in, h_in):
+            d.copy_(h, non_blocking=True)
+        M.mla_kv_write(cache, d_in[0], d_in[1], d_in[2])
+        M.mla_sparse_decode(d_in[3], cache, d_in[4], db.sm_scale, out=out_d, lse=lse_d, workspace=ws)
+        h_out.copy_(out_d, non_blocking=True)
+        h_lse.copy_(lse_d, non_blocking=True)
+        e1.record()
+        e1.synchronize()
+        if k >= 2:
+            e2e_ms.append(e0.elapsed_time(e1))
+
+    # reduce: max over ranks of the summed device time
+    tot = torch.tensor([sum(s_ms), sum(w_ms), sum(d_ms), sum(e2e_ms)], dtype=torch.float64, device=dev)
+    if world > 1:
+        torch.distributed.all_reduce(tot, op=torch.distributed.ReduceOp.MAX)
+    step_ms, writer_ms, decode_ms, e2e_tot = (tot / torch.tensor([K, K, K, len(e2e_ms)], device=dev,
+                                                                  dtype=torch.float64)).tolist()
+
+    n_valid = int((db.topk > 0).sum())
+    n_written = int((wb.slot_idx > 0).sum())
+    gathered = n_valid * 656
+    decode_alg = gathered + db.T * db.W * 4 + db.T * db.H * 576 * 2 + db.T * db.H * 512 * 2 + db.T * db.H * 4
+    writer_alg = n_written * (1024 + 128 + 656) + wb.slot_idx.numel() * 8
+    peak, peak_kind = load_peaks()
+    achieved = decode_alg / (decode_ms * 1e-3) / 1e9
+    traffic = recorded_traffic()
+
+    result = None
+    if rank == 0:
+        cpu = None
+        if world == 1 and not args.no_cpu_baseline:
+            cache_np = cache.cpu().numpy()
+            cpu = oracle_cpu_baseline(wl, cache_np, wb, seconds=args.cpu_seconds)
+        result = {
+            "metric": METRIC,
+            "value": world * db.T / (step_ms * 1e-3),
+            "unit": UNIT,
+            "n_gpus": world,
+            "steps": K,
+            "warmup": args.warmup,
+            "ms_per_step": step_ms,
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "e4m3 cache; bf16 q/out; f16/bf16 tensor-core MMA with fp32 accumulate",
+            "data": "synthetic (seeded N(0,1) bf16; no model weights)",
+            "config": {
+                "workload": "writer sweep + saturated decode: 1,048,576-slot cache of 656-B rows; per step "
+                            "mla_kv_write of 8,192 rows (random 25% aimed at slot 0) then mla_sparse_decode "
+                            "T=256, H=16, d_qk=576, top-k 2,048 all present, sm_scale=1/sqrt(576)",
+                "T": db.T, "H": db.H, "d_qk": db.d_qk, "topk": db.W, "num_slots": wl.num_slots,
+                "writer_rows": int(wb.slot_idx.numel()), "writer_rows_written": n_written,
+                "l2": "flushed between timed steps (256 MiB write, outside the timed events)",
+                "timing": "CUDA events on the launching stream around each step; device time summed over steps",
+            },
+            "decode": {
+                "us": decode_ms * 1e3,
+                "query_tokens_per_s": world * db.T / (decode_ms * 1e-3),
+                "gathered_kv_gbs": gathered / (decode_ms * 1e-3) / 1e9,
+                "gathered_bytes": gathered,
+                "nsplit_workspace_bytes": 0 if ws is None else int(ws.numel()),
+            },
+            "writer": {
+                "us": writer_ms * 1e3,
+                "rows_per_s": world * wb.slot_idx.numel() / (writer_ms * 1e-3),
+                "algorithmic_gbs": writer_alg / (writer_ms * 1e-3) / 1e9,
+                "hbm_frac": writer_alg / (writer_ms * 1e-3) / 1e9 / peak,
+            },
+            "roofline": {
+                "kernel": "mla_sparse_decode_kernel (+ split combine)",
+                "bound": "hbm",
+                "achieved": achieved,
+                "peak": peak,
+                "unit": "GB/s",
+                "frac": achieved / peak,
+                "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)" if peak_kind == "measured" else "fallback 6.8 TB/s",
+                "algorithmic_bytes_per_launch": decode_alg,
+                "traffic": traffic,
+            },
+            "clocks": clocks,
+            "e2e": {
+                "value": world * db.T / (e2e_tot * 1e-3),
+                "unit": UNIT,
+                "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_tot,
+            },
+            "gpu_launches": K * launches_per_step,
+            "cpu_baseline": cpu,
+            "wall_s_timed_region": wall,
+        }
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+    return result
+
+
+def run_reference(args, rank, world):
+    """CPU oracle arm: each step writes the 8,192-row batch with the oracle
+    writer and decodes a bounded sample of the query tokens with the oracle."""
+    if rank != 0:
+        return None
+    import oracle
+    oracle.build()
+    wl = workloads.sweep()
+    wb = next(w for w in wl.writes if w.label == WRITE_LABEL)
+    db = wl.decode
+    cache = np.full((wl.num_slots, 656), wl.slot0_byte, np.uint8)
+    oracle.kv_write(cache, wl.fill.slot_idx.numpy(), wl.fill.latent, wl.fill.rope)
+    cores = oracle.default_threads()
+    topk = db.topk.numpy()
+    per_step = max(1, min(db.T, cores))
+    times = []
+    for k in range(args.warmup + args.steps):
+        toks = [(k * per_step + i) % db.T for i in range(per_step)]
+        t0 = time.perf_counter()
+        oracle.kv_write(cache, wb.slot_idx.numpy(), wb.latent, wb.rope)
+        oracle.sparse_decode(db.q, cache, topk, db.sm_scale, tokens=toks, n_threads=cores)
+        dt = time.perf_counter() - t0
+        if k >= args.warmup:
+            times.append(dt)
+    total = sum(times)
+    value = per_step * len(times) / total
+    return {
+        "impl": "reference",
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * total / len(times), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)", "data": "synthetic",
+        "config": {"workload": "same as the GPU arm; per step the oracle writes the 8,192-row batch and "
+                               f"decodes {per_step} of the 256 query tokens",
+                   "T": db.T, "H": db.H, "d_qk": db.d_qk, "topk": db.W, "num_slots": wl.num_slots},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"{per_step} query tokens + the 8,192-row write per step"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    rank, world, local_rank = dist_env()
+    if args.impl == "reference":
+        res = run_reference(args, rank, world)
+    else:
+        res = run_ours(args, rank, world, local_rank)
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,109 @@
+// mla_kv_write: per-token FP8 quantise-and-scatter into packed 656-byte rows.
+//
+// Follows vLLM PR #55277 (Purpose item 1: the fp8_ds_mla row = 512 B latent +
+// 16 B tile scales + 128 B RoPE or zero padding; pe_dim in {64, 0}) and sglang
+// PR #47013 (Summary / Modifications: rows aimed at the reserved slot are
+// dropped; Motivation: the quantiser keeps BF16 NaNs).
+//
+// One warp per row. Lane l owns latent values 16l .. 16l+15 (two 16-byte
+// loads), so tile t = lanes 8t .. 8t+7 and the tile amax is a 3-step xor
+// shuffle. The 512 FP8 bytes leave in one fully coalesced 16-byte store per
+// lane; lanes 0..7 then store the 128-byte tail and lane 8 the 16 bytes of
+// scales (bytes 512..655 in one instruction). A dropped row costs its 8-byte
+// slot index and nothing else.
+#include "mla_device.cuh"
+
+namespace {
+
+using namespace mla;
+
+constexpr int kWriterThreads = 256;   // 8 rows in flight per CTA
+
+__device__ __forceinline__ uint32_t quant2(float x0, float x1, float scale) {
+    // IEEE fp32 division, then round-to-nearest-even E4M3 with saturation.
+    const float2 v = make_float2(__fdiv_rn(x0, scale), __fdiv_rn(x1, scale));
+    return static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(v, __NV_SATFINITE, __NV_E4M3));
+}
+
+__global__ void __launch_bounds__(kWriterThreads)
+mla_kv_write_kernel(uint8_t* __restrict__ cache, int64_t num_slots,
+                    const int64_t* __restrict__ slot_idx,
+                    const uint16_t* __restrict__ latent,
+                    const uint16_t* __restrict__ rope,
+                    int64_t n_rows, int64_t reserved_slot, int* __restrict__ err) {
+    const int lane = threadIdx.x & 31;
+    const int64_t stride = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    for (int64_t r = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; r < n_rows;
+         r += stride) {
+        const int64_t slot = __ldg(slot_idx + r);            // same for the whole warp
+        if (slot == reserved_slot || slot < 0) continue;     // dropped: no input is read
+        if (slot >= num_slots) {
+            if (lane == 0) atomicOr(err, MLA_ERR_WRITE_SLOT_RANGE);
+            continue;
+        }
+        const uint8_t* src = reinterpret_cast<const uint8_t*>(latent + r * kLatent) + 32 * lane;
+        const uint4 a = ld_nc_v4(src);
+        const uint4 b = ld_nc_v4(src + 16);
+        uint4 tail = make_uint4(0u, 0u, 0u, 0u);
+        if (rope != nullptr && lane < 8)
+            tail = ld_nc_v4(reinterpret_cast<const uint8_t*>(rope + r * kRope) + 16 * lane);
+
+        const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+        float v[16];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            v[2 * i] = bf16lo(w[i]);
+            v[2 * i + 1] = bf16hi(w[i]);
+        }
+        float amax = 0.0f;                                   // fmaxf ignores NaN
+#pragma unroll
+        for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
+        const float scale = (amax > 0.0f) ? __fdiv_rn(amax, MLA_FP8_MAX) : 1.0f;
+
+        uint32_t qv[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            qv[k] = quant2(v[4 * k], v[4 * k + 1], scale) | (quant2(v[4 * k + 2], v[4 * k + 3], scale) << 16);
+
+        uint8_t* row = cache + slot * static_cast<int64_t>(kRowBytes);
+        st_v4(row + 16 * lane, make_uint4(qv[0], qv[1], qv[2], qv[3]));
+        const float s0 = __shfl_sync(0xffffffffu, scale, 0);
+        const float s1 = __shfl_sync(0xffffffffu, scale, 8);
+        const float s2 = __shfl_sync(0xffffffffu, scale, 16);
+        const float s3 = __shfl_sync(0xffffffffu, scale, 24);
+        if (lane < 8) {
+            st_v4(row + kTailOff + 16 * lane, tail);
+        } else if (lane == 8) {
+            st_v4(row + kScaleOff, make_uint4(__float_as_uint(s0), __float_as_uint(s1),
+                                              __float_as_uint(s2), __float_as_uint(s3)));
+        }
+    }
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+extern "C" int mla_kv_write(mla_kv_cache_t kv, const int64_t* slot_idx, const void* latent_bf16,
+                            const void* rope_bf16, int64_t n_rows, int64_t reserved_slot, void* stream) {
+    if (n_rows < 0 || kv.row_bytes != MLA_ROW_BYTES || kv.num_slots < 0) return MLA_EINVAL;
+    if (n_rows == 0) return MLA_OK;
+    if (kv.data == nullptr || slot_idx == nullptr || latent_bf16 == nullptr) return MLA_EINVAL;
+    if (!aligned16(kv.data) || !aligned16(latent_bf16) || (rope_bf16 && !aligned16(rope_bf16)) ||
+        (reinterpret_cast<uintptr_t>(slot_idx) & 7u))
+        return MLA_EINVAL;
+    int* err = mla_host::device_error_word();
+    const int sms = mla_host::sm_count();
+    if (err == nullptr || sms <= 0) return MLA_ECUDA;
+    const int64_t rows_per_cta = kWriterThreads / 32;
+    int64_t blocks = (n_rows + rows_per_cta - 1) / rows_per_cta;
+    const int64_t max_blocks = static_cast<int64_t>(sms) * 8;     // 64 resident warps per SM
+    if (blocks > max_blocks) blocks = max_blocks;
+    mla_kv_write_kernel<<<static_cast<unsigned>(blocks), kWriterThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<uint8_t*>(kv.data), kv.num_slots, slot_idx, static_cast<const uint16_t*>(latent_bf16),
+        static_cast<const uint16_t*>(rope_bf16), n_rows, reserved_slot, err);
+    return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ECUDA;
+}

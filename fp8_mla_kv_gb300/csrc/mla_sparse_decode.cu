@@ -1,0 +1,554 @@
+// mla_sparse_decode: sparse top-k MLA decode over the packed FP8 cache.
+//
+// What it computes follows the decode statement quoted in the C header, with
+// the masking rule of sglang PR #39288 (Root cause: a -1 candidate must add
+// nothing and must not gather slot 0) and sglang PR #47013 (Motivation: masking
+// only the score does not stop a NaN row). Here an absent entry is removed
+// before anything is fetched: each CTA compacts its slice of the top-k list in
+// shared memory, so -1, slot 0 and out-of-range indices are never dereferenced.
+//
+// Work decomposition: one CTA per (token, split of the top-k list, group of 16
+// heads); 4 warps; warp w owns latent tile w (dims 128w .. 128w+127) and RoPE
+// dims 16w .. 16w+15. Present rows move global -> shared with one
+// cp.async.bulk per row (656 B, or 528 B for NoPE: the tail is not read) into
+// a 4-stage ring of 32-row blocks, each stage completing on an mbarrier.
+//
+// Arithmetic per 32-row block, on tensor cores (m16n8k16, heads as M):
+//   QK  : the E4M3 latent goes to f16 exactly (cvt.f16x2.e4m3x2); q goes to f16
+//         exactly after an exponent-only per-head rescale that keeps it in f16
+//         range; the per-row, per-tile fp32 scale multiplies each warp's tile
+//         partial afterwards, so the product q.K is exact before fp32
+//         accumulation. RoPE dims run as a bf16 MMA on the stored bf16 values.
+//   softmax: the four tile partials are summed through shared memory; online
+//         max / sum in fp32 with exp2 (log2 e folded into sm_scale).
+//   PV  : p * scale_row / sigma (sigma = running max of the tile's scales, so the
+//         f16 operand stays in [0, 1]) times the exact f16 E4M3 codes; O stays
+//         in registers (16 heads x 128 dims per warp) and is rescaled with the
+//         softmax correction.
+// Splits write a normalised partial (o, lse) to the caller's workspace and a
+// second kernel merges them in split order (deterministic: no float atomics).
+#include <cfloat>
+#include <cmath>
+
+#include "mla_device.cuh"
+
+namespace {
+
+using namespace mla;
+
+constexpr int kHeads = 16;                   // heads per CTA (M of m16n8k16)
+constexpr int kWarps = 4;
+constexpr int kThreads = kWarps * 32;
+constexpr int kNB = 32;                      // rows per block
+constexpr int kStages = 4;
+constexpr int kListMax = 2304;               // positions one CTA compacts
+constexpr int kStageBytes = kNB * kRowBytes; // 20,992
+constexpr int kSmemStages = kStages * kStageBytes;
+constexpr int kSmemList = kListMax * 4;
+constexpr int kSmemRed = kWarps * 32 * 16 * 4;
+constexpr int kSmemQmax = kWarps * kHeads * 4;
+constexpr int kSmemMisc = 64;                 // warp counts + barriers
+constexpr int kSmemTotal = kSmemStages + kSmemList + kSmemRed + kSmemQmax + kSmemMisc;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+struct DecodeArgs {
+    const __nv_bfloat16* q;
+    const uint8_t* cache;
+    const int32_t* topk;
+    __nv_bfloat16* out;
+    float* lse;
+    float* ws_o;      // [T, nsplit, H, 512] (nsplit > 1)
+    float* ws_lse;    // [T, nsplit, H]
+    int* err;
+    int64_t num_slots;
+    int T, H, d_qk, W, nsplit, split_len;
+    float sm_scale_log2;   // sm_scale * log2(e)
+};
+
+__global__ void __launch_bounds__(kThreads, 2)
+mla_sparse_decode_kernel(const DecodeArgs args) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint8_t* stages = smem;
+    int* list = reinterpret_cast<int*>(smem + kSmemStages);
+    float* red = reinterpret_cast<float*>(smem + kSmemStages + kSmemList);
+    float* qmax_s = reinterpret_cast<float*>(smem + kSmemStages + kSmemList + kSmemRed);
+    int* wcount = reinterpret_cast<int*>(smem + kSmemStages + kSmemList + kSmemRed + kSmemQmax);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(wcount + 8);
+
+    const int t = blockIdx.x;
+    const int split = blockIdx.y;
+    const int hg = blockIdx.z;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int g = lane >> 2;
+    const int c = lane & 3;
+    const int H = args.H;
+    const bool with_rope = (args.d_qk == kLatent + kRope);
+    const uint32_t row_read = with_rope ? kRowBytes : kNopeReadBytes;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) mbar_init(&bars[s], 1);
+        fence_mbar_init();
+    }
+
+    // ---- 1. compact the present entries of this split's positions ----
+    const int p0 = split * args.split_len;
+    const int p1 = min(args.W, p0 + args.split_len);
+    const int32_t* trow = args.topk + static_cast<int64_t>(t) * args.W;
+    int n_valid = 0;
+    for (int base = p0; base < p1; base += kThreads) {
+        const int pos = base + threadIdx.x;
+        const int idx = (pos < p1) ? __ldg(trow + pos) : -1;
+        const bool valid = idx > 0 && static_cast<int64_t>(idx) < args.num_slots;
+        if (idx > 0 && !valid) atomicOr(args.err, MLA_ERR_DECODE_INDEX_RANGE);
+        const unsigned m = __ballot_sync(0xffffffffu, valid);
+        if (lane == 0) wcount[warp] = __popc(m);
+        __syncthreads();
+        int off = n_valid;
+        int total = 0;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+            const int cw = wcount[w];
+            off += (w < warp) ? cw : 0;
+            total += cw;
+        }
+        if (valid) list[off + __popc(m & ((1u << lane) - 1u))] = idx;
+        n_valid += total;
+        __syncthreads();
+    }
+    const int nblk = (n_valid + kNB - 1) / kNB;
+
+    // ---- 2. start the gathers (warp 0 issues; lane j copies row j of a block) ----
+    auto issue = [&](int b) {
+        const int s = b % kStages;
+        uint8_t* dst = stages + s * kStageBytes;
+        const int n_b = min(kNB, n_valid - b * kNB);
+        if (n_b < kNB) {
+            // Rows past the end of the list load nothing; zero them so the
+            // block's arithmetic sees finite zeros (E4M3 0 and scale 0.0).
+            if (lane >= n_b) {
+                uint4* z = reinterpret_cast<uint4*>(dst + lane * kRowBytes);
+                for (int k = 0; k < kRowBytes / 16; ++k) z[k] = make_uint4(0u, 0u, 0u, 0u);
+            }
+            fence_proxy_async_smem();
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive_expect_tx(&bars[s], static_cast<uint32_t>(n_b) * row_read);
+        __syncwarp();
+        if (lane < n_b)
+            bulk_g2s(dst + lane * kRowBytes,
+                     args.cache + static_cast<int64_t>(list[b * kNB + lane]) * kRowBytes, row_read, &bars[s]);
+    };
+    __syncthreads();   // barrier init visible
+    if (warp == 0) {
+        for (int b = 0; b < min(kStages, nblk); ++b) issue(b);
+    }
+
+    // ---- 3. q fragments (overlaps the first gathers) ----
+    const int h_lo = hg * kHeads + g;
+    const int h_hi = h_lo + 8;
+    uint32_t qraw[2][16];
+    uint32_t qr[2][2];
+    float qm[2];
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+        const int h = r ? h_hi : h_lo;
+        qm[r] = 0.0f;
+        if (h < H) {
+            const __nv_bfloat16* qh = args.q + (static_cast<int64_t>(t) * H + h) * args.d_qk;
+            const uint8_t* p = reinterpret_cast<const uint8_t*>(qh + 128 * warp + 32 * c);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const uint4 v = ld_nc_v4(p + 16 * k);
+                qraw[r][4 * k + 0] = v.x; qraw[r][4 * k + 1] = v.y;
+                qraw[r][4 * k + 2] = v.z; qraw[r][4 * k + 3] = v.w;
+            }
+            if (with_rope) {
+                const uint2 v = *reinterpret_cast<const uint2*>(qh + kLatent + 16 * warp + 4 * c);
+                qr[r][0] = v.x; qr[r][1] = v.y;
+            } else {
+                qr[r][0] = qr[r][1] = 0u;
+            }
+        } else {
+#pragma unroll
+            for (int k = 0; k < 16; ++k) qraw[r][k] = 0u;
+            qr[r][0] = qr[r][1] = 0u;
+        }
+#pragma unroll
+        for (int k = 0; k < 16; ++k) qm[r] = fmaxf(qm[r], fmaxf(fabsf(bf16lo(qraw[r][k])), fabsf(bf16hi(qraw[r][k]))));
+#pragma unroll
+        for (int k = 0; k < 2; ++k) qm[r] = fmaxf(qm[r], fmaxf(fabsf(bf16lo(qr[r][k])), fabsf(bf16hi(qr[r][k]))));
+        qm[r] = fmaxf(qm[r], __shfl_xor_sync(0xffffffffu, qm[r], 1));
+        qm[r] = fmaxf(qm[r], __shfl_xor_sync(0xffffffffu, qm[r], 2));
+    }
+    if (c == 0) {
+        qmax_s[warp * kHeads + g] = qm[0];
+        qmax_s[warp * kHeads + g + 8] = qm[1];
+    }
+    __syncthreads();
+    // Exponent-only rescale so that |q| < 2^15 in f16: exact whenever q is in
+    // f16's normal range after the shift; the shift is undone on the scores.
+    float qdown[2], qup[2];
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+        float mx = 0.0f;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) mx = fmaxf(mx, qmax_s[w * kHeads + g + 8 * r]);
+        int e = 0;
+        frexpf(mx, &e);                              // mx < 2^e
+        const int k = (e > 15) ? (e - 15) : 0;
+        qdown[r] = ldexpf(1.0f, -k);
+        qup[r] = ldexpf(1.0f, k);
+    }
+    uint32_t qa[8][4];      // f16 A fragments of the 8 k-steps of this warp's tile
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+            const int wi = 8 * hf + 2 * kk;
+            qa[4 * hf + kk][0] = pack_f16x2(bf16lo(qraw[0][wi]) * qdown[0], bf16hi(qraw[0][wi]) * qdown[0]);
+            qa[4 * hf + kk][1] = pack_f16x2(bf16lo(qraw[1][wi]) * qdown[1], bf16hi(qraw[1][wi]) * qdown[1]);
+            qa[4 * hf + kk][2] = pack_f16x2(bf16lo(qraw[0][wi + 1]) * qdown[0], bf16hi(qraw[0][wi + 1]) * qdown[0]);
+            qa[4 * hf + kk][3] = pack_f16x2(bf16lo(qraw[1][wi + 1]) * qdown[1], bf16hi(qraw[1][wi + 1]) * qdown[1]);
+        }
+    }
+    const uint32_t qra[4] = {qr[0][0], qr[1][0], qr[0][1], qr[1][1]};
+
+    // ---- 4. main loop ----
+    float o[16][4];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.0f;
+    float m_run[2] = {-INFINITY, -INFINITY};
+    float l_run[2] = {0.0f, 0.0f};
+    float sigma = FLT_MIN;
+    const float sl2 = args.sm_scale_log2;
+
+    for (int b = 0; b < nblk; ++b) {
+        const int s = b % kStages;
+        const bool ok = mbar_wait_bounded(&bars[s], static_cast<uint32_t>((b / kStages) & 1));
+        if (__syncthreads_or(!ok)) {
+            // A copy did not land in time: record it, drain what is still in
+            // flight (bounded as well) and leave without touching the outputs.
+            if (threadIdx.x == 0) {
+                atomicOr(args.err, MLA_ERR_PIPELINE_TIMEOUT);
+                for (int bb = b; bb < min(nblk, b + kStages); ++bb)
+                    (void)mbar_wait_bounded(&bars[bb % kStages], static_cast<uint32_t>((bb / kStages) & 1));
+            }
+            __syncthreads();
+            return;
+        }
+        const uint8_t* st = stages + s * kStageBytes;
+        const int n_b = min(kNB, n_valid - b * kNB);
+
+        // QK^T: latent on f16 MMA, RoPE on bf16 MMA.
+        float acc[4][4], accr[4][4];
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) acc[nt][i] = accr[nt][i] = 0.0f;
+            const uint8_t* rowp = st + (nt * 8 + g) * kRowBytes;
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                const uint4 kv = *reinterpret_cast<const uint4*>(rowp + 128 * warp + 32 * c + 16 * hf);
+                const uint32_t kw[4] = {kv.x, kv.y, kv.z, kv.w};
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_f16(acc[nt], qa[4 * hf + kk], e4m3x2_to_f16x2(kw[kk]), e4m3x2_to_f16x2(kw[kk] >> 16));
+            }
+            if (with_rope) {
+                const uint2 rb = *reinterpret_cast<const uint2*>(rowp + kTailOff + 32 * warp + 8 * c);
+                mma_bf16(accr[nt], qra, rb.x, rb.y);
+            }
+        }
+        // Per-row tile scale (rows past n_b were zero-filled: scale 0).
+        float sc[4][2];
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e)
+                sc[nt][e] = *reinterpret_cast<const float*>(st + (nt * 8 + 2 * c + e) * kRowBytes + kScaleOff + 4 * warp);
+        // Reduction buffer as float4 [warp][nt][lane]: conflict-free 16-byte accesses.
+        float4* red4 = reinterpret_cast<float4*>(red);
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt) {
+            float4 v;
+            v.x = acc[nt][0] * (sc[nt][0] * qup[0]) + accr[nt][0];
+            v.y = acc[nt][1] * (sc[nt][1] * qup[0]) + accr[nt][1];
+            v.z = acc[nt][2] * (sc[nt][0] * qup[1]) + accr[nt][2];
+            v.w = acc[nt][3] * (sc[nt][1] * qup[1]) + accr[nt][3];
+            red4[(warp * 4 + nt) * 32 + lane] = v;
+        }
+        __syncthreads();
+        float sfull[4][4];
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt) {
+            float4 a = red4[nt * 32 + lane];
+#pragma unroll
+            for (int w = 1; w < kWarps; ++w) {
+                const float4 bq = red4[(w * 4 + nt) * 32 + lane];
+                a.x += bq.x; a.y += bq.y; a.z += bq.z; a.w += bq.w;
+            }
+            sfull[nt][0] = a.x; sfull[nt][1] = a.y; sfull[nt][2] = a.z; sfull[nt][3] = a.w;
+        }
+
+        // Online softmax in log2 units; columns past n_b are absent.
+        float rmax[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int j = nt * 8 + 2 * c + (i & 1);
+                const float v = (j < n_b) ? sfull[nt][i] * sl2 : -INFINITY;
+                sfull[nt][i] = v;
+                rmax[i >> 1] = fmaxf(rmax[i >> 1], v);
+            }
+        }
+        float alpha[2], m_use[2];
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            rmax[r] = fmaxf(rmax[r], __shfl_xor_sync(0xffffffffu, rmax[r], 1));
+            rmax[r] = fmaxf(rmax[r], __shfl_xor_sync(0xffffffffu, rmax[r], 2));
+            const float m_new = fmaxf(m_run[r], rmax[r]);
+            m_use[r] = (m_new == -INFINITY) ? 0.0f : m_new;
+            alpha[r] = exp2f(m_run[r] - m_use[r]);
+            m_run[r] = m_new;
+        }
+        float psum[2] = {0.0f, 0.0f};
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float p = exp2f(sfull[nt][i] - m_use[i >> 1]);
+                sfull[nt][i] = p;
+                psum[i >> 1] += p;
+            }
+        }
+        l_run[0] = l_run[0] * alpha[0] + psum[0];
+        l_run[1] = l_run[1] * alpha[1] + psum[1];
+
+        // Running max of this tile's scales keeps the f16 P operand in [0, 1].
+        const float sblk = warp_max((lane < n_b)
+            ? *reinterpret_cast<const float*>(st + lane * kRowBytes + kScaleOff + 4 * warp) : 0.0f);
+        const float sig_new = fmaxf(sigma, sblk);
+        const float rs = sigma / sig_new;
+        const float inv = 1.0f / sig_new;
+        sigma = sig_new;
+        const float f0 = alpha[0] * rs, f1 = alpha[1] * rs;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            o[i][0] *= f0; o[i][1] *= f0; o[i][2] *= f1; o[i][3] *= f1;
+        }
+        uint32_t pa[2][4];
+#pragma unroll
+        for (int kb = 0; kb < 2; ++kb) {
+            const int n0 = 2 * kb, n1 = 2 * kb + 1;
+            const float a0 = sc[n0][0] * inv, a1 = sc[n0][1] * inv, b0 = sc[n1][0] * inv, b1 = sc[n1][1] * inv;
+            pa[kb][0] = pack_f16x2(sfull[n0][0] * a0, sfull[n0][1] * a1);
+            pa[kb][1] = pack_f16x2(sfull[n0][2] * a0, sfull[n0][3] * a1);
+            pa[kb][2] = pack_f16x2(sfull[n1][0] * b0, sfull[n1][1] * b1);
+            pa[kb][3] = pack_f16x2(sfull[n1][2] * b0, sfull[n1][3] * b1);
+        }
+
+        // PV: V rows j as K, dims of tile `warp` as N.
+#pragma unroll
+        for (int kb = 0; kb < 2; ++kb) {
+            const uint8_t* vb = st + 128 * warp + 4 * g;
+            const int j0 = 16 * kb + 2 * c;
+#pragma unroll
+            for (int qd = 0; qd < 4; ++qd) {
+                const uint32_t W0 = *reinterpret_cast<const uint32_t*>(vb + (j0 + 0) * kRowBytes + 32 * qd);
+                const uint32_t W1 = *reinterpret_cast<const uint32_t*>(vb + (j0 + 1) * kRowBytes + 32 * qd);
+                const uint32_t W2 = *reinterpret_cast<const uint32_t*>(vb + (j0 + 8) * kRowBytes + 32 * qd);
+                const uint32_t W3 = *reinterpret_cast<const uint32_t*>(vb + (j0 + 9) * kRowBytes + 32 * qd);
+                const uint32_t p01a = prmt(W0, W1, 0x5140), p01b = prmt(W0, W1, 0x7362);
+                const uint32_t p23a = prmt(W2, W3, 0x5140), p23b = prmt(W2, W3, 0x7362);
+                mma_f16(o[4 * qd + 0], pa[kb], e4m3x2_to_f16x2(p01a), e4m3x2_to_f16x2(p23a));
+                mma_f16(o[4 * qd + 1], pa[kb], e4m3x2_to_f16x2(p01a >> 16), e4m3x2_to_f16x2(p23a >> 16));
+                mma_f16(o[4 * qd + 2], pa[kb], e4m3x2_to_f16x2(p01b), e4m3x2_to_f16x2(p23b));
+                mma_f16(o[4 * qd + 3], pa[kb], e4m3x2_to_f16x2(p01b >> 16), e4m3x2_to_f16x2(p23b >> 16));
+            }
+        }
+        __syncthreads();          // stage s and the reduction buffer are free again
+        if (warp == 0 && b + kStages < nblk) issue(b + kStages);
+    }
+
+    // ---- 5. epilogue ----
+    float lt[2];
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+        float l = l_run[r];
+        l += __shfl_xor_sync(0xffffffffu, l, 1);
+        l += __shfl_xor_sync(0xffffffffu, l, 2);
+        lt[r] = l;
+    }
+    const float mult[2] = {lt[0] > 0.0f ? sigma / lt[0] : 0.0f, lt[1] > 0.0f ? sigma / lt[1] : 0.0f};
+    const float lse_r[2] = {lt[0] > 0.0f ? (m_run[0] + log2f(lt[0])) * kLn2 : -INFINITY,
+                            lt[1] > 0.0f ? (m_run[1] + log2f(lt[1])) * kLn2 : -INFINITY};
+    const int hs[2] = {h_lo, h_hi};
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+        const int h = hs[r];
+        if (h >= H) continue;
+        const int i0 = 2 * r, i1 = 2 * r + 1;
+        if (args.nsplit == 1) {
+            __nv_bfloat16* orow = args.out + (static_cast<int64_t>(t) * H + h) * kLatent + 128 * warp + 8 * c;
+#pragma unroll
+            for (int qd = 0; qd < 4; ++qd) {
+                const float mm = mult[r];
+                uint4 v;
+                v.x = pack_bf16x2(o[4 * qd + 0][i0] * mm, o[4 * qd + 1][i0] * mm);
+                v.y = pack_bf16x2(o[4 * qd + 2][i0] * mm, o[4 * qd + 3][i0] * mm);
+                v.z = pack_bf16x2(o[4 * qd + 0][i1] * mm, o[4 * qd + 1][i1] * mm);
+                v.w = pack_bf16x2(o[4 * qd + 2][i1] * mm, o[4 * qd + 3][i1] * mm);
+                st_v4(orow + 32 * qd, v);
+            }
+            if (warp == 0 && c == 0) args.lse[static_cast<int64_t>(t) * H + h] = lse_r[r];
+        } else {
+            const int64_t prow = (static_cast<int64_t>(t) * args.nsplit + split) * H + h;
+            float* orow = args.ws_o + prow * kLatent + 128 * warp + 8 * c;
+#pragma unroll
+            for (int qd = 0; qd < 4; ++qd) {
+                const float mm = mult[r];
+                const float4 v0 = make_float4(o[4 * qd + 0][i0] * mm, o[4 * qd + 1][i0] * mm,
+                                              o[4 * qd + 2][i0] * mm, o[4 * qd + 3][i0] * mm);
+                const float4 v1 = make_float4(o[4 * qd + 0][i1] * mm, o[4 * qd + 1][i1] * mm,
+                                              o[4 * qd + 2][i1] * mm, o[4 * qd + 3][i1] * mm);
+                reinterpret_cast<float4*>(orow + 32 * qd)[0] = v0;
+                reinterpret_cast<float4*>(orow + 32 * qd)[1] = v1;
+            }
+            if (warp == 0 && c == 0) args.ws_lse[prow] = lse_r[r];
+        }
+    }
+}
+
+// Merge of the split partials of one (token, head): lse = ln sum_s exp(lse_s),
+// out = sum_s exp(lse_s - lse) o_s, in split order.
+__global__ void __launch_bounds__(128)
+mla_split_combine_kernel(const float* __restrict__ ws_o, const float* __restrict__ ws_lse,
+                         int H, int nsplit, __nv_bfloat16* __restrict__ out, float* __restrict__ lse) {
+    const int64_t th = blockIdx.x;              // t * H + h
+    const int64_t t = th / H;
+    const int h = static_cast<int>(th % H);
+    float mx = -INFINITY;
+    for (int s = 0; s < nsplit; ++s) mx = fmaxf(mx, ws_lse[(t * nsplit + s) * H + h]);
+    const int d = 4 * threadIdx.x;
+    __nv_bfloat16* orow = out + th * kLatent + d;
+    if (mx == -INFINITY) {
+        *reinterpret_cast<uint2*>(orow) = make_uint2(0u, 0u);
+        if (threadIdx.x == 0) lse[th] = -INFINITY;
+        return;
+    }
+    float wsum = 0.0f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s = 0; s < nsplit; ++s) {
+        const int64_t prow = (t * nsplit + s) * H + h;
+        const float ls = ws_lse[prow];
+        if (ls == -INFINITY) continue;
+        const float w = expf(ls - mx);
+        wsum += w;
+        const float4 v = *reinterpret_cast<const float4*>(ws_o + prow * kLatent + d);
+        acc.x += w * v.x; acc.y += w * v.y; acc.z += w * v.z; acc.w += w * v.w;
+    }
+    const float inv = 1.0f / wsum;
+    *reinterpret_cast<uint2*>(orow) = make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv),
+                                                 pack_bf16x2(acc.z * inv, acc.w * inv));
+    if (threadIdx.x == 0) lse[th] = mx + logf(wsum);
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Number of splits of each token's top-k list: enough CTAs for about four per
+// SM, at least 64 positions per split, and at most kListMax positions per split.
+int choose_nsplit(int T, int H, int W, int sms) {
+    if (T <= 0 || W <= 0) return 1;
+    const int64_t base = static_cast<int64_t>(T) * ((H + kHeads - 1) / kHeads);
+    const int64_t target = 4ll * sms;
+    int64_t ns = (target + base - 1) / base;
+    const int64_t max_ns = (W >= 64) ? W / 64 : 1;
+    if (ns > max_ns) ns = max_ns;
+    const int64_t min_ns = (W + kListMax - 1) / kListMax;
+    if (ns < min_ns) ns = min_ns;
+    if (ns < 1) ns = 1;
+    return static_cast<int>(ns);
+}
+
+size_t workspace_for(int T, int H, int nsplit) {
+    if (nsplit <= 1) return 0;
+    const size_t rows = static_cast<size_t>(T) * nsplit * H;
+    const size_t o_bytes = rows * kLatent * sizeof(float);
+    return o_bytes + ((rows * sizeof(float) + 255) & ~static_cast<size_t>(255));
+}
+
+}  // namespace
+
+extern "C" size_t mla_sparse_decode_workspace_bytes(int T, int H, int W) {
+    if (T <= 0 || H <= 0 || H > 128 || W < 0) return 0;
+    const int sms = mla_host::sm_count();
+    if (sms <= 0) return 0;
+    return workspace_for(T, H, choose_nsplit(T, H, W, sms));
+}
+
+extern "C" int mla_sparse_decode(const void* q_bf16, int T, int H, int d_qk, mla_kv_cache_t kv,
+                                 const int32_t* topk_idx, int W, float sm_scale, void* out_bf16,
+                                 float* lse, void* workspace, size_t workspace_bytes, void* stream) {
+    if (T < 0 || W < 0 || kv.row_bytes != MLA_ROW_BYTES || kv.num_slots < 0 || !std::isfinite(sm_scale))
+        return MLA_EINVAL;
+    if (d_qk != kLatent && d_qk != kLatent + kRope) return MLA_EUNSUPPORTED;
+    if (H < 1 || H > 128) return MLA_EUNSUPPORTED;
+    if (T == 0) return MLA_OK;
+    if (q_bf16 == nullptr || out_bf16 == nullptr || lse == nullptr || (W > 0 && topk_idx == nullptr) ||
+        (W > 0 && kv.data == nullptr))
+        return MLA_EINVAL;
+    if (!aligned16(q_bf16) || !aligned16(out_bf16) || (kv.data && !aligned16(kv.data)) ||
+        (reinterpret_cast<uintptr_t>(lse) & 3u) || (reinterpret_cast<uintptr_t>(topk_idx) & 3u))
+        return MLA_EINVAL;
+    int* err = mla_host::device_error_word();
+    const int sms = mla_host::sm_count();
+    if (err == nullptr || sms <= 0) return MLA_ECUDA;
+    const int nsplit = choose_nsplit(T, H, W, sms);
+    const size_t need = workspace_for(T, H, nsplit);
+    if (need > 0 && (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)))
+        return MLA_ENOWORKSPACE;
+
+    static bool attr_set[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MLA_ECUDA;
+    if (!attr_set[dev]) {
+        if (cudaFuncSetAttribute(mla_sparse_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kSmemTotal) != cudaSuccess)
+            return MLA_ECUDA;
+        attr_set[dev] = true;
+    }
+    DecodeArgs a;
+    a.q = static_cast<const __nv_bfloat16*>(q_bf16);
+    a.cache = static_cast<const uint8_t*>(kv.data);
+    a.topk = topk_idx;
+    a.out = static_cast<__nv_bfloat16*>(out_bf16);
+    a.lse = lse;
+    a.ws_o = static_cast<float*>(workspace);
+    a.ws_lse = nsplit > 1 ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
+                                                     static_cast<size_t>(T) * nsplit * H * kLatent * sizeof(float))
+                          : nullptr;
+    a.err = err;
+    a.num_slots = kv.num_slots;
+    a.T = T; a.H = H; a.d_qk = d_qk; a.W = W; a.nsplit = nsplit;
+    a.split_len = (W + nsplit - 1) / nsplit;
+    a.sm_scale_log2 = sm_scale * kLog2e;
+    const dim3 grid(static_cast<unsigned>(T), static_cast<unsigned>(nsplit), static_cast<unsigned>((H + kHeads - 1) / kHeads));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    mla_sparse_decode_kernel<<<grid, kThreads, kSmemTotal, st>>>(a);
+    if (cudaGetLastError() != cudaSuccess) return MLA_ECUDA;
+    if (nsplit > 1) {
+        mla_split_combine_kernel<<<static_cast<unsigned>(static_cast<int64_t>(T) * H), 128, 0, st>>>(
+            a.ws_o, a.ws_lse, H, nsplit, a.out, a.lse);
+        if (cudaGetLastError() != cudaSuccess) return MLA_ECUDA;
+    }
+    return MLA_OK;
+}

@@ -1,0 +1,169 @@
+/*
+ * libmlasparse - FP8 MLA KV cache writer and sparse top-k MLA decode on one
+ * GB300 GPU (sm_103a). Plain C ABI: device pointers, sizes, a CUDA stream.
+ *
+ * Row layout (vLLM PR #55277 "Support NoPE sparse MLA (GLM-5.3-Flash) on the
+ * FlashInfer SM120 backend", Purpose item 1): every cache slot is one 656-byte
+ * row
+ *     bytes [  0, 512)  512 E4M3 latent values, value i at byte i, in four
+ *                       tiles of 128 values (tile t = bytes 128t .. 128t+127)
+ *     bytes [512, 528)  four little-endian fp32 tile scales, tile t at 512 + 4t
+ *     bytes [528, 656)  64 bf16 RoPE values, or 128 zero bytes for NoPE rows
+ * and a stored value decodes as e4m3(byte) * scale[tile].
+ *
+ * Slot 0 is reserved (sglang PR #47013 "zero-RoPE writer skips reserved slot 0",
+ * Summary and Motivation): the allocators never hand it out, padding rows aim
+ * at it, and no write may land there.
+ *
+ * Conventions for every entry point:
+ *   - All array arguments are DEVICE pointers on the current CUDA device, owned
+ *     by the caller; the library never allocates, frees or retains them.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *     stream). Calls are asynchronous on that stream.
+ *   - The return value is MLA_OK (0) or a negative MLA_E* code; arguments are
+ *     validated on the host before any launch and nothing is launched on error.
+ *     No C++ exception crosses this boundary.
+ *   - Range violations found on the device (a slot or a top-k index past the
+ *     cache) never trap: the row or entry is dropped and a bit is set in the
+ *     library's device error word, read with mla_get_error().
+ */
+#ifndef MLASPARSE_H
+#define MLASPARSE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- row layout (vLLM PR #55277, Purpose item 1) ---- */
+#define MLA_ROW_BYTES      656
+#define MLA_LATENT_DIM     512
+#define MLA_TILE_VALUES    128
+#define MLA_NUM_TILES      4
+#define MLA_SCALE_OFFSET   512
+#define MLA_TAIL_OFFSET    528
+#define MLA_ROPE_DIM       64
+#define MLA_FP8_MAX        448.0f   /* largest finite E4M3 value */
+
+/* ---- return codes ---- */
+#define MLA_OK             0
+#define MLA_EINVAL        (-1)   /* null pointer, negative size, misaligned pointer, bad layout */
+#define MLA_EUNSUPPORTED  (-2)   /* d_qk not in {512, 576}, H outside [1, 128] */
+#define MLA_ENOWORKSPACE  (-3)   /* workspace NULL or smaller than mla_sparse_decode_workspace_bytes() */
+#define MLA_ECUDA         (-4)   /* a CUDA runtime call or a kernel launch failed */
+
+/* ---- device error word bits (mla_get_error) ---- */
+#define MLA_ERR_WRITE_SLOT_RANGE   0x1  /* mla_kv_write: slot >= num_slots, row dropped */
+#define MLA_ERR_DECODE_INDEX_RANGE 0x2  /* mla_sparse_decode: index >= num_slots, entry absent */
+#define MLA_ERR_PIPELINE_TIMEOUT   0x4  /* a kernel's bounded wait on its own copies ran out */
+
+/* A cache: `data` is a device array of num_slots rows of row_bytes bytes,
+ * 16-byte aligned. row_bytes must be MLA_ROW_BYTES. */
+typedef struct {
+    void*   data;
+    int64_t num_slots;
+    int64_t row_bytes;
+} mla_kv_cache_t;
+
+/*
+ * mla_kv_write - per-token FP8 quantise-and-scatter into packed rows.
+ *
+ * Defined by vLLM PR #55277 (Purpose item 1: the 656-byte row; NoPE rows zero
+ * the 128-byte tail; pe_dim must be 64 or 0) and sglang PR #47013 (Summary,
+ * Motivation, Modifications: rows aimed at the reserved slot are dropped; BF16
+ * NaNs are kept by the quantiser, not clamped).
+ *
+ * For each row r in [0, n_rows) with s = slot_idx[r]:
+ *   - s == reserved_slot or s < 0: the row is dropped and none of its inputs is
+ *     read (its latent may hold NaN);
+ *   - s >= kv.num_slots: the row is dropped and MLA_ERR_WRITE_SLOT_RANGE is set;
+ *   - otherwise row s of the cache is overwritten: for each tile t,
+ *       scale_t = amax_t / 448 (IEEE fp32 division; 1.0 when amax_t == 0;
+ *                 amax ignores NaN),
+ *       byte    = e4m3 round-to-nearest-even, saturating to +-448, of x / scale_t
+ *                 (IEEE fp32 division; a NaN x gives the NaN code 0x7F),
+ *     the four scales go to bytes 512..527, and bytes 528..655 receive rope row r
+ *     verbatim, or zeros when rope_bf16 is NULL.
+ * No other byte of the cache is touched.
+ *
+ * Arguments:
+ *   kv            cache (device, 16-byte aligned, row_bytes == 656)
+ *   slot_idx      int64 [n_rows], device
+ *   latent_bf16   bf16 [n_rows, 512] row-major, device, 16-byte aligned
+ *   rope_bf16     bf16 [n_rows, 64] row-major, device, 16-byte aligned; or NULL
+ *                 for pe_dim = 0 (NoPE)
+ *   n_rows        >= 0 (0 launches nothing)
+ *   reserved_slot the slot writes must never land in (0 in every caller)
+ * Precondition: no two rows of one call name the same non-reserved slot (which
+ * of them would land is unspecified).
+ * Returns MLA_OK, MLA_EINVAL or MLA_ECUDA.
+ */
+int mla_kv_write(mla_kv_cache_t kv, const int64_t* slot_idx, const void* latent_bf16,
+                 const void* rope_bf16, int64_t n_rows, int64_t reserved_slot, void* stream);
+
+/*
+ * mla_sparse_decode_workspace_bytes - bytes of device workspace that
+ * mla_sparse_decode needs for these sizes on the CURRENT device (the split of
+ * the top-k list across CTAs depends on the device's SM count). 0 means no
+ * workspace is needed. Returns 0 for invalid sizes as well.
+ */
+size_t mla_sparse_decode_workspace_bytes(int T, int H, int W);
+
+/*
+ * mla_sparse_decode - sparse top-k MLA decode over the packed FP8 cache.
+ *
+ * Defined by the benchmark spec of the decode together with sglang PR #47013
+ * (Motivation: unused top-k entries must not reach the result, even when slot 0
+ * holds NaN), sglang PR #39288 ("SM120 sparse MLA: zero-initialise the
+ * page-split scratch", Root cause: a -1 candidate contributes nothing and must
+ * not gather slot 0), and vLLM PR #55277 (Purpose item 2: the index buffer
+ * width W is a capacity; the active entries are bounded by the -1 padding;
+ * Purpose item 1 and "Relation to #53969": NoPE decode reads no tail).
+ *
+ * For each token t < T and head h < H, with J = { j : 0 < topk_idx[t,j] <
+ * kv.num_slots } (-1 or any negative, the reserved slot 0, and out-of-range
+ * indices are absent: never dereferenced, contributing nothing; an index >=
+ * num_slots also sets MLA_ERR_DECODE_INDEX_RANGE):
+ *   s_j       = sm_scale * ( q[t,h,0:512] . K_j  +  [d_qk == 576] q[t,h,512:576] . rope_j )
+ *   K_j[d]    = e4m3(byte_d of row) * scale[d / 128]      (V_j = K_j)
+ *   out[t,h]  = sum_j softmax(s)_j V_j                     (bf16)
+ *   lse[t,h]  = ln sum_j exp(s_j)                          (fp32, natural log)
+ * An empty J gives out = 0 and lse = -inf. The result does not depend on the
+ * order of the entries nor on what slot 0 holds (bit-identical output).
+ *
+ * Arguments:
+ *   q_bf16     bf16 [T, H, d_qk] row-major, device, 16-byte aligned
+ *   T, H       tokens (>= 0; 0 launches nothing) and heads (1..128)
+ *   d_qk       576 (512 latent + 64 RoPE) or 512 (NoPE: the row tail is not read)
+ *   kv         the cache (row_bytes == 656, 16-byte aligned)
+ *   topk_idx   int32 [T, W] row-major, device; W >= 0
+ *   sm_scale   softmax scale applied to q . k (finite)
+ *   out_bf16   bf16 [T, H, 512] row-major, device, 16-byte aligned
+ *   lse        fp32 [T, H], device
+ *   workspace  device scratch of at least mla_sparse_decode_workspace_bytes(T,H,W)
+ *              bytes, 16-byte aligned (may be NULL when that is 0). Its contents
+ *              on entry do not matter; it is clobbered.
+ * Returns MLA_OK, MLA_EINVAL, MLA_EUNSUPPORTED, MLA_ENOWORKSPACE or MLA_ECUDA.
+ */
+int mla_sparse_decode(const void* q_bf16, int T, int H, int d_qk, mla_kv_cache_t kv,
+                      const int32_t* topk_idx, int W, float sm_scale, void* out_bf16,
+                      float* lse, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * mla_get_error - read and clear the device error word of the current device
+ * (MLA_ERR_* bits accumulated by every launch since the last read). Blocks
+ * until the device is idle. Returns MLA_OK or MLA_ECUDA; *host_code receives
+ * the bits (host pointer, not NULL).
+ */
+int mla_get_error(int32_t* host_code);
+
+/* Human-readable name of a return code (static string). */
+const char* mla_strerror(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLASPARSE_H */
