@@ -27,7 +27,7 @@
 // notes):
 //   * tile scale = amax / 448 in IEEE fp32 (round to nearest), 1.0 if amax == 0;
 //   * value = e4m3_rne_satfinite(x / scale), the division in IEEE fp32;
-//   * amax ignores NaN (fmax); a NaN element encodes as 0x7F;
+//   * amax ignores every NaN (quiet or signaling); a NaN element encodes as 0x7F;
 //   * +-inf saturates to +-448 (0x7E / 0xFE), like any out-of-range value;
 //   * latent value i is stored at byte i; tile t holds bytes 128t .. 128t+127;
 //   * scales are four little-endian fp32 at bytes 512 + 4t;
@@ -160,10 +160,13 @@ int64_t oracle_kv_write(uint8_t* cache, int64_t num_slots, const int64_t* slot_i
         uint8_t* row = cache + slot * kRowBytes;
         const uint16_t* x = latent_bf16 + r * kLatent;
         for (int t = 0; t < kTiles; ++t) {
-            // Step 2: tile amax, NaN-ignoring.
+            // Step 2: tile amax, ignoring every NaN (quiet or signaling: a bf16 NaN
+            // whose top mantissa bit is clear widens to a signaling fp32 NaN).
             float amax = 0.0f;
-            for (int i = 0; i < kTileValues; ++i)
-                amax = std::fmax(amax, std::fabs(bf16_to_float(x[t * kTileValues + i])));
+            for (int i = 0; i < kTileValues; ++i) {
+                const float a = std::fabs(bf16_to_float(x[t * kTileValues + i]));
+                if (!std::isnan(a) && a > amax) amax = a;
+            }
             // Step 3: fp32 scale.
             const float scale = (amax > 0.0f) ? (amax / 448.0f) : 1.0f;
             // Step 4: quantise value i of tile t to byte 128t + i.

@@ -138,3 +138,23 @@ def test_slot0_kept_whatever_it_holds():
         oracle.kv_write(cache, wb.slot_idx.numpy(), wb.latent, wb.rope)
         assert np.all(cache[0] == fill)
         assert int((wb.slot_idx == 0).sum()) == 32
+
+
+def test_amax_ignores_quiet_and_signaling_nans():
+    # "per-token FP8 quantization keeps BF16 NaNs" (sglang PR #47013, Motivation):
+    # NaN elements encode as NaN and do not enter the tile amax, whether the bf16
+    # NaN widens to a quiet (0x7FC1) or a signaling (0x7F97) fp32 NaN.
+    bits = np.zeros((1, 512), np.uint16)
+    bits[0, 0] = 0x43E0                       # 448.0
+    bits[0, 1:40] = 0x7F97                    # signaling after widening
+    bits[0, 40:60] = 0xFFC1                   # quiet, negative
+    bits[0, 60:70] = 0x0015                   # bf16 subnormal
+    bits[0, 128] = 0x7F81
+    bits[0, 129] = 0x3F80                     # 1.0
+    lat = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16)
+    cache = np.zeros((2, 656), np.uint8)
+    oracle.kv_write(cache, np.array([1]), lat, None)
+    sc = _scales(cache[1])
+    assert sc[0] == 1.0 and sc[1] == np.float32(1.0) / np.float32(448.0)
+    assert np.all(cache[1, 1:60] == 0x7F) and cache[1, 128] == 0x7F
+    assert cache[1, 0] == 0x7E and cache[1, 129] == 0x7E
