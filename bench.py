@@ -145,10 +145,39 @@ def oracle_cpu_baseline(wl, cache_np, wb, seconds: float = 12.0):
                       f"(H={db.H}, W={db.W}, all present) in {dt:.2f} s on {cores} threads"}
 
 
+WORKLOADS = {
+    # default: writer sweep + saturated decode at full size
+    "sweep": (lambda: workloads.sweep(),
+              "writer sweep + saturated decode: 1,048,576-slot cache of 656-B rows; per step mla_kv_write of "
+              "8,192 rows (random 25% aimed at slot 0) then mla_sparse_decode T=256, H=16, d_qk=576, top-k "
+              "2,048 all present, sm_scale=1/sqrt(576)"),
+    # reduced case of the same kernels for ncu captures (cache 172 MB > L2)
+    "sweep-small": (lambda: workloads.sweep(num_slots=262144, T=64),
+                    "reduced sweep for profiling: 262,144-slot cache; 8,192-row padded write; decode T=64, "
+                    "H=16, top-k 2,048"),
+    "nope": (lambda: workloads.nope(),
+             "NoPE decode: 131,072-slot cache, T=64, H=16, d_qk=512, W=2,176, active length U(1..2048)"),
+    "rope": (lambda: workloads.rope(),
+             "RoPE decode: 1,048,576-slot cache with 1% x20 outliers, T=128, H=64, d_qk=576, top-k 2,048"),
+    "prefill": (lambda: workloads.prefill(),
+                "prefill-shaped: 65,536-slot paged cache, T=1,024 causal rows, H=16, W=2,048"),
+    "tiny": (lambda: workloads.tiny(), "tiny end-to-end: 4,096 slots, 288-row write, T=4, H=16, W=128"),
+}
+
+
+def step_write_batch(wl):
+    for w in wl.writes:
+        if w.label == WRITE_LABEL:
+            return w
+    return wl.writes[0] if wl.writes else None
+
+
 def build_cache_gpu(wl, dev):
     from fp8_mla_kv_gb300 import mlasparse as M
     cache = torch.full((wl.num_slots, 656), wl.slot0_byte, dtype=torch.uint8, device=dev)
     f = wl.fill
+    if f is None:
+        return cache
     chunk = 1 << 18
     for r0 in range(0, f.slot_idx.shape[0], chunk):
         r1 = min(f.slot_idx.shape[0], r0 + chunk)
@@ -168,22 +197,29 @@ def run_ours(args, rank, world, local_rank):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
 
-    wl = workloads.sweep()
-    wb = next(w for w in wl.writes if w.label == WRITE_LABEL)
+    make_wl, wl_desc = WORKLOADS[args.workload]
+    wl = make_wl()
+    wb = step_write_batch(wl)
     db = wl.decode
     cache = build_cache_gpu(wl, dev)
 
-    slots_d, lat_d, rope_d = wb.slot_idx.to(dev), wb.latent.to(dev), wb.rope.to(dev)
+    if wb is not None:
+        slots_d, lat_d = wb.slot_idx.to(dev), wb.latent.to(dev)
+        rope_d = None if wb.rope is None else wb.rope.to(dev)
     q_d, topk_d = db.q.to(dev), db.topk.to(dev)
     out_d = torch.empty((db.T, db.H, 512), dtype=torch.bfloat16, device=dev)
     lse_d = torch.empty((db.T, db.H), dtype=torch.float32, device=dev)
     ws = M.alloc_workspace(db.T, db.H, db.W, dev)
-    launches_per_step = 1 + 1 + (1 if ws is not None else 0)
+    launches_per_step = (1 if wb is not None else 0) + 1 + (1 if ws is not None else 0)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
 
+    def write():
+        if wb is not None:
+            M.mla_kv_write(cache, slots_d, lat_d, rope_d)
+
     def step():
-        M.mla_kv_write(cache, slots_d, lat_d, rope_d)
+        write()
         M.mla_sparse_decode(q_d, cache, topk_d, db.sm_scale, out=out_d, lse=lse_d, workspace=ws)
 
     for _ in range(args.warmup):
@@ -203,7 +239,7 @@ def run_ours(args, rank, world, local_rank):
     for k in range(K):
         flush.zero_()                      # L2 flushed between timed steps (not timed)
         ev[k][0].record()
-        M.mla_kv_write(cache, slots_d, lat_d, rope_d)
+        write()
         ev[k][1].record()
         M.mla_sparse_decode(q_d, cache, topk_d, db.sm_scale, out=out_d, lse=lse_d, workspace=ws)
         ev[k][2].record()
@@ -219,28 +255,32 @@ def run_ours(args, rank, world, local_rank):
 
     # End to end through the public API with pinned host buffers: per step the
     # inputs go host -> device, the outputs come back device -> host.
-    h_in = [t.pin_memory() for t in (wb.slot_idx, wb.latent, wb.rope, db.q, db.topk)]
+    w_in = [] if wb is None else [t for t in (wb.slot_idx, wb.latent, wb.rope) if t is not None]
+    h_in = [t.pin_memory() for t in w_in + [db.q, db.topk]]
     h_out = torch.empty((db.T, db.H, 512), dtype=torch.bfloat16).pin_memory()
     h_lse = torch.empty((db.T, db.H), dtype=torch.float32).pin_memory()
     d_in = [torch.empty_like(t, device=dev) for t in h_in]
     h2d = sum(t.numel() * t.element_size() for t in h_in)
     d2h = h_out.numel() * 2 + h_lse.numel() * 4
-    e2e_steps = max(3, min(K, 200))
+    e2e_steps = 0 if args.no_e2e else max(3, min(K, 200))
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e2e_ms = []
-    for k in range(e2e_steps + 2):
+    for k in range(e2e_steps + 2 if e2e_steps else 0):
         flush.zero_()
         e0.record()
         for d, h in zip(d_in, h_in):
             d.copy_(h, non_blocking=True)
-        M.mla_kv_write(cache, d_in[0], d_in[1], d_in[2])
-        M.mla_sparse_decode(d_in[3], cache, d_in[4], db.sm_scale, out=out_d, lse=lse_d, workspace=ws)
+        if wb is not None:
+            M.mla_kv_write(cache, d_in[0], d_in[1], d_in[2] if len(w_in) == 3 else None)
+        M.mla_sparse_decode(d_in[-2], cache, d_in[-1], db.sm_scale, out=out_d, lse=lse_d, workspace=ws)
         h_out.copy_(out_d, non_blocking=True)
         h_lse.copy_(lse_d, non_blocking=True)
         e1.record()
         e1.synchronize()
         if k >= 2:
             e2e_ms.append(e0.elapsed_time(e1))
+    if not e2e_ms:
+        e2e_ms = [float("nan")]
 
     # reduce: max over ranks of the summed device time
     tot = torch.tensor([sum(s_ms), sum(w_ms), sum(d_ms), sum(e2e_ms)], dtype=torch.float64, device=dev)
@@ -249,11 +289,14 @@ def run_ours(args, rank, world, local_rank):
     step_ms, writer_ms, decode_ms, e2e_tot = (tot / torch.tensor([K, K, K, len(e2e_ms)], device=dev,
                                                                   dtype=torch.float64)).tolist()
 
-    n_valid = int((db.topk > 0).sum())
-    n_written = int((wb.slot_idx > 0).sum())
-    gathered = n_valid * 656
-    decode_alg = gathered + db.T * db.W * 4 + db.T * db.H * 576 * 2 + db.T * db.H * 512 * 2 + db.T * db.H * 4
-    writer_alg = n_written * (1024 + 128 + 656) + wb.slot_idx.numel() * 8
+    n_valid = int(((db.topk > 0) & (db.topk < wl.num_slots)).sum())
+    row_read = 656 if db.d_qk == 576 else 528
+    gathered = n_valid * row_read
+    decode_alg = (gathered + db.T * db.W * 4 + db.T * db.H * db.d_qk * 2 + db.T * db.H * 512 * 2
+                  + db.T * db.H * 4)
+    n_rows = 0 if wb is None else int(wb.slot_idx.numel())
+    n_written = 0 if wb is None else int((wb.slot_idx > 0).sum())
+    writer_alg = n_written * (1024 + (128 if wb is not None and wb.rope is not None else 0) + 656) + n_rows * 8
     peak, peak_kind = load_peaks()
     achieved = decode_alg / (decode_ms * 1e-3) / 1e9
     traffic = recorded_traffic()
@@ -261,7 +304,7 @@ def run_ours(args, rank, world, local_rank):
     result = None
     if rank == 0:
         cpu = None
-        if world == 1 and not args.no_cpu_baseline:
+        if world == 1 and not args.no_cpu_baseline and args.workload == "sweep":
             cache_np = cache.cpu().numpy()
             cpu = oracle_cpu_baseline(wl, cache_np, wb, seconds=args.cpu_seconds)
         result = {
@@ -278,11 +321,10 @@ def run_ours(args, rank, world, local_rank):
             "dtype": "e4m3 cache; bf16 q/out; f16/bf16 tensor-core MMA with fp32 accumulate",
             "data": "synthetic (seeded N(0,1) bf16; no model weights)",
             "config": {
-                "workload": "writer sweep + saturated decode: 1,048,576-slot cache of 656-B rows; per step "
-                            "mla_kv_write of 8,192 rows (random 25% aimed at slot 0) then mla_sparse_decode "
-                            "T=256, H=16, d_qk=576, top-k 2,048 all present, sm_scale=1/sqrt(576)",
+                "workload": wl_desc,
                 "T": db.T, "H": db.H, "d_qk": db.d_qk, "topk": db.W, "num_slots": wl.num_slots,
-                "writer_rows": int(wb.slot_idx.numel()), "writer_rows_written": n_written,
+                "present_entries": n_valid,
+                "writer_rows": n_rows, "writer_rows_written": n_written,
                 "l2": "flushed between timed steps (256 MiB write, outside the timed events)",
                 "timing": "CUDA events on the launching stream around each step; device time summed over steps",
             },
@@ -293,9 +335,9 @@ def run_ours(args, rank, world, local_rank):
                 "gathered_bytes": gathered,
                 "nsplit_workspace_bytes": 0 if ws is None else int(ws.numel()),
             },
-            "writer": {
+            "writer": None if wb is None else {
                 "us": writer_ms * 1e3,
-                "rows_per_s": world * wb.slot_idx.numel() / (writer_ms * 1e-3),
+                "rows_per_s": world * n_rows / (writer_ms * 1e-3),
                 "algorithmic_gbs": writer_alg / (writer_ms * 1e-3) / 1e9,
                 "hbm_frac": writer_alg / (writer_ms * 1e-3) / 1e9 / peak,
             },
@@ -308,7 +350,7 @@ def run_ours(args, rank, world, local_rank):
                 "frac": achieved / peak,
                 "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)" if peak_kind == "measured" else "fallback 6.8 TB/s",
                 "algorithmic_bytes_per_launch": decode_alg,
-                "traffic": traffic,
+                "traffic": traffic if args.workload == "sweep" else None,
             },
             "clocks": clocks,
             "e2e": {
@@ -376,6 +418,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="sweep")
     args = ap.parse_args()
     rank, world, local_rank = dist_env()
     if args.impl == "reference":
