@@ -152,6 +152,38 @@ int mla_sparse_decode(const void* q_bf16, int T, int H, int d_qk, mla_kv_cache_t
                       float* lse, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * mla_sparse_decode_noalloc - mla_sparse_decode for callers that cannot
+ * allocate device memory where they call it.
+ *
+ * The pages have no counterpart to this entry point; it exists for users of
+ * this library. mla_sparse_decode needs a caller-owned workspace whenever it
+ * splits a token's top-k list across CTAs (mla_sparse_decode_workspace_bytes()
+ * > 0). A caller that runs inside another framework's memory pool without an
+ * allocator handle, or a process that has already committed all the device
+ * memory it may use, has no way to provide one. This variant computes exactly
+ * what mla_sparse_decode computes, with the same arguments minus the
+ * workspace, and uses instead a fixed array of MLA_NOALLOC_SCRATCH_BYTES in the
+ * library's own device memory. That array exists on every GPU that loads the
+ * library's device code and stays allocated until the process exits. The call
+ * allocates nothing (no cudaMalloc, cudaFree or allocating library routine).
+ *
+ *   - Sizes whose workspace would exceed MLA_NOALLOC_SCRATCH_BYTES are rejected
+ *     with MLA_ENOWORKSPACE before anything is launched.
+ *   - All calls on a device share the one array and it keeps what the last call
+ *     left there: calls whose work overlaps on the GPU (other streams, or
+ *     concurrently replayed graphs) race and produce wrong results. Issue them
+ *     on one stream. Nothing in the array needs to start at zero.
+ *   - The first call on a device looks up the array's address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ * Returns what mla_sparse_decode returns.
+ */
+#define MLA_NOALLOC_SCRATCH_BYTES (64u << 20)   /* 64 MiB per device */
+int mla_sparse_decode_noalloc(const void* q_bf16, int T, int H, int d_qk, mla_kv_cache_t kv,
+                              const int32_t* topk_idx, int W, float sm_scale, void* out_bf16,
+                              float* lse, void* stream);
+
+/*
  * mla_get_error - read and clear the device error word of the current device
  * (MLA_ERR_* bits accumulated by every launch since the last read). Blocks
  * until the device is idle. Returns MLA_OK or MLA_ECUDA; *host_code receives
