@@ -37,25 +37,29 @@ namespace {
 using namespace mla;
 
 constexpr int kHeads = 16;                   // heads per CTA (M of m16n8k16)
-constexpr int kWarps = 4;
-constexpr int kThreads = kWarps * 32;
+constexpr int kWarps = 4;                    // consumer warps (one per latent tile)
+constexpr int kProducer = kWarps;            // warp index of the copy-issuing warp
+constexpr int kThreads = (kWarps + 1) * 32;
+constexpr int kConsumerThreads = kWarps * 32;
 constexpr int kNB = 32;                      // rows per block
 constexpr int kStages = 4;
 constexpr int kListMax = 2304;               // positions one CTA compacts
 constexpr int kStageBytes = kNB * kRowBytes; // 20,992
 constexpr int kSmemStages = kStages * kStageBytes;
 constexpr int kSmemList = kListMax * 4;
-constexpr int kSmemRed = kWarps * 32 * 16 * 4;
+constexpr int kSmemRed = 2 * kWarps * 4 * 32 * 16;   // two buffers of float4 [warp][n-tile][lane]
 constexpr int kSmemQmax = kWarps * kHeads * 4;
-constexpr int kSmemMisc = 64;                 // warp counts + barriers
+constexpr int kSmemMisc = 16 + 2 * kStages * 8 + 16; // warp counts, full + empty barriers, issued count
 constexpr int kSmemTotal = kSmemStages + kSmemList + kSmemRed + kSmemQmax + kSmemMisc;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
+// The running max used as the exp2 offset is only moved when a score exceeds it
+// by more than this (log2 units): p <= 2^8 keeps the f16 P operand in range.
+constexpr float kRescaleSlack = 8.0f;
 
-__device__ __forceinline__ float warp_max(float v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-    return v;
+__device__ __forceinline__ float quad_max(float v) {
+    v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 1));
+    return fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 2));
 }
 
 struct DecodeArgs {
@@ -72,47 +76,50 @@ struct DecodeArgs {
     float sm_scale_log2;   // sm_scale * log2(e)
 };
 
+template <bool kRopeOn>
 __global__ void __launch_bounds__(kThreads, 2)
 mla_sparse_decode_kernel(const DecodeArgs args) {
     extern __shared__ __align__(128) uint8_t smem[];
     uint8_t* stages = smem;
     int* list = reinterpret_cast<int*>(smem + kSmemStages);
-    float* red = reinterpret_cast<float*>(smem + kSmemStages + kSmemList);
+    float4* red = reinterpret_cast<float4*>(smem + kSmemStages + kSmemList);
     float* qmax_s = reinterpret_cast<float*>(smem + kSmemStages + kSmemList + kSmemRed);
     int* wcount = reinterpret_cast<int*>(smem + kSmemStages + kSmemList + kSmemRed + kSmemQmax);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(wcount + 8);
+    uint64_t* full = reinterpret_cast<uint64_t*>(wcount + 4);
+    uint64_t* empty = full + kStages;
+    int* issued_s = reinterpret_cast<int*>(empty + kStages);
 
     const int t = blockIdx.x;
     const int split = blockIdx.y;
     const int hg = blockIdx.z;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int g = lane >> 2;
-    const int c = lane & 3;
     const int H = args.H;
-    const bool with_rope = (args.d_qk == kLatent + kRope);
-    const uint32_t row_read = with_rope ? kRowBytes : kNopeReadBytes;
+    constexpr uint32_t kRowRead = kRopeOn ? kRowBytes : kNopeReadBytes;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) mbar_init(&bars[s], 1);
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kWarps);
+        }
+        *issued_s = 0;
         fence_mbar_init();
     }
 
-    // ---- 1. compact the present entries of this split's positions ----
+    // ---- 1. compact the present entries of this split's positions (all warps) ----
     const int p0 = split * args.split_len;
     const int p1 = min(args.W, p0 + args.split_len);
     const int32_t* trow = args.topk + static_cast<int64_t>(t) * args.W;
     int n_valid = 0;
-    for (int base = p0; base < p1; base += kThreads) {
+    for (int base = p0; base < p1; base += kConsumerThreads) {
         const int pos = base + threadIdx.x;
-        const int idx = (pos < p1) ? __ldg(trow + pos) : -1;
+        const int idx = (warp < kWarps && pos < p1) ? __ldg(trow + pos) : -1;
         const bool valid = idx > 0 && static_cast<int64_t>(idx) < args.num_slots;
         if (idx > 0 && !valid) atomicOr(args.err, MLA_ERR_DECODE_INDEX_RANGE);
         const unsigned m = __ballot_sync(0xffffffffu, valid);
-        if (lane == 0) wcount[warp] = __popc(m);
+        if (lane == 0 && warp < kWarps) wcount[warp] = __popc(m);
         __syncthreads();
-        int off = n_valid;
-        int total = 0;
+        int off = n_valid, total = 0;
 #pragma unroll
         for (int w = 0; w < kWarps; ++w) {
             const int cw = wcount[w];
@@ -125,33 +132,41 @@ mla_sparse_decode_kernel(const DecodeArgs args) {
     }
     const int nblk = (n_valid + kNB - 1) / kNB;
 
-    // ---- 2. start the gathers (warp 0 issues; lane j copies row j of a block) ----
-    auto issue = [&](int b) {
-        const int s = b % kStages;
-        uint8_t* dst = stages + s * kStageBytes;
-        const int n_b = min(kNB, n_valid - b * kNB);
-        if (n_b < kNB) {
-            // Rows past the end of the list load nothing; zero them so the
-            // block's arithmetic sees finite zeros (E4M3 0 and scale 0.0).
-            if (lane >= n_b) {
-                uint4* z = reinterpret_cast<uint4*>(dst + lane * kRowBytes);
-                for (int k = 0; k < kRowBytes / 16; ++k) z[k] = make_uint4(0u, 0u, 0u, 0u);
+    if (warp == kProducer) {
+        // ---- producer: lane j copies row j of each block into the stage ring ----
+        int b = 0;
+        for (; b < nblk; ++b) {
+            const int s = b % kStages;
+            if (b >= kStages && !mbar_wait_bounded(&empty[s], static_cast<uint32_t>(((b / kStages) - 1) & 1))) {
+                if (lane == 0) atomicOr(args.err, MLA_ERR_PIPELINE_TIMEOUT);
+                break;
             }
-            fence_proxy_async_smem();
+            uint8_t* dst = stages + s * kStageBytes;
+            const int n_b = min(kNB, n_valid - b * kNB);
+            if (n_b < kNB) {
+                // Rows past the end of the list load nothing: zero them so the
+                // block's arithmetic sees finite zeros (E4M3 0, scale 0.0).
+                if (lane >= n_b) {
+                    uint4* z = reinterpret_cast<uint4*>(dst + lane * kRowBytes);
+                    for (int k = 0; k < kRowBytes / 16; ++k) z[k] = make_uint4(0u, 0u, 0u, 0u);
+                }
+                fence_proxy_async_smem();
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(n_b) * kRowRead);
+            __syncwarp();
+            if (lane < n_b)
+                bulk_g2s(dst + lane * kRowBytes,
+                         args.cache + static_cast<int64_t>(list[b * kNB + lane]) * kRowBytes, kRowRead, &full[s]);
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive_expect_tx(&bars[s], static_cast<uint32_t>(n_b) * row_read);
-        __syncwarp();
-        if (lane < n_b)
-            bulk_g2s(dst + lane * kRowBytes,
-                     args.cache + static_cast<int64_t>(list[b * kNB + lane]) * kRowBytes, row_read, &bars[s]);
-    };
-    __syncthreads();   // barrier init visible
-    if (warp == 0) {
-        for (int b = 0; b < min(kStages, nblk); ++b) issue(b);
+        if (lane == 0) *issued_s = b;
+        __syncthreads();     // matches the consumers' final barrier
+        return;
     }
 
-    // ---- 3. q fragments (overlaps the first gathers) ----
+    // ---- consumers: q fragments ----
+    const int g = lane >> 2;
+    const int c = lane & 3;
     const int h_lo = hg * kHeads + g;
     const int h_hi = h_lo + 8;
     uint32_t qraw[2][16];
@@ -161,6 +176,7 @@ mla_sparse_decode_kernel(const DecodeArgs args) {
     for (int r = 0; r < 2; ++r) {
         const int h = r ? h_hi : h_lo;
         qm[r] = 0.0f;
+        qr[r][0] = qr[r][1] = 0u;
         if (h < H) {
             const __nv_bfloat16* qh = args.q + (static_cast<int64_t>(t) * H + h) * args.d_qk;
             const uint8_t* p = reinterpret_cast<const uint8_t*>(qh + 128 * warp + 32 * c);
@@ -170,32 +186,29 @@ mla_sparse_decode_kernel(const DecodeArgs args) {
                 qraw[r][4 * k + 0] = v.x; qraw[r][4 * k + 1] = v.y;
                 qraw[r][4 * k + 2] = v.z; qraw[r][4 * k + 3] = v.w;
             }
-            if (with_rope) {
+            if (kRopeOn) {
                 const uint2 v = *reinterpret_cast<const uint2*>(qh + kLatent + 16 * warp + 4 * c);
                 qr[r][0] = v.x; qr[r][1] = v.y;
-            } else {
-                qr[r][0] = qr[r][1] = 0u;
             }
         } else {
 #pragma unroll
             for (int k = 0; k < 16; ++k) qraw[r][k] = 0u;
-            qr[r][0] = qr[r][1] = 0u;
         }
 #pragma unroll
         for (int k = 0; k < 16; ++k) qm[r] = fmaxf(qm[r], fmaxf(fabsf(bf16lo(qraw[r][k])), fabsf(bf16hi(qraw[r][k]))));
 #pragma unroll
         for (int k = 0; k < 2; ++k) qm[r] = fmaxf(qm[r], fmaxf(fabsf(bf16lo(qr[r][k])), fabsf(bf16hi(qr[r][k]))));
-        qm[r] = fmaxf(qm[r], __shfl_xor_sync(0xffffffffu, qm[r], 1));
-        qm[r] = fmaxf(qm[r], __shfl_xor_sync(0xffffffffu, qm[r], 2));
+        qm[r] = quad_max(qm[r]);
     }
     if (c == 0) {
         qmax_s[warp * kHeads + g] = qm[0];
         qmax_s[warp * kHeads + g + 8] = qm[1];
     }
-    __syncthreads();
-    // Exponent-only rescale so that |q| < 2^15 in f16: exact whenever q is in
-    // f16's normal range after the shift; the shift is undone on the scores.
-    float qdown[2], qup[2];
+    bar_sync_or(1, kConsumerThreads, false);
+    // Exponent-only rescale so that |q| < 2^15 in f16 (exact in f16's normal
+    // range); the same power of two scales the RoPE part, and is undone on the
+    // scores through the per-row softmax factor.
+    float qdown[2], rowf[2];
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
         float mx = 0.0f;
@@ -205,9 +218,9 @@ mla_sparse_decode_kernel(const DecodeArgs args) {
         frexpf(mx, &e);                              // mx < 2^e
         const int k = (e > 15) ? (e - 15) : 0;
         qdown[r] = ldexpf(1.0f, -k);
-        qup[r] = ldexpf(1.0f, k);
+        rowf[r] = args.sm_scale_log2 * ldexpf(1.0f, k);
     }
-    uint32_t qa[8][4];      // f16 A fragments of the 8 k-steps of this warp's tile
+    uint32_t qa[8][4];
 #pragma unroll
     for (int hf = 0; hf < 2; ++hf) {
 #pragma unroll
@@ -219,141 +232,140 @@ mla_sparse_decode_kernel(const DecodeArgs args) {
             qa[4 * hf + kk][3] = pack_f16x2(bf16lo(qraw[1][wi + 1]) * qdown[1], bf16hi(qraw[1][wi + 1]) * qdown[1]);
         }
     }
-    const uint32_t qra[4] = {qr[0][0], qr[1][0], qr[0][1], qr[1][1]};
+    uint32_t qra[4];
+    qra[0] = pack_bf16x2(bf16lo(qr[0][0]) * qdown[0], bf16hi(qr[0][0]) * qdown[0]);
+    qra[1] = pack_bf16x2(bf16lo(qr[1][0]) * qdown[1], bf16hi(qr[1][0]) * qdown[1]);
+    qra[2] = pack_bf16x2(bf16lo(qr[0][1]) * qdown[0], bf16hi(qr[0][1]) * qdown[0]);
+    qra[3] = pack_bf16x2(bf16lo(qr[1][1]) * qdown[1], bf16hi(qr[1][1]) * qdown[1]);
 
-    // ---- 4. main loop ----
+    // ---- consumers: main loop ----
     float o[16][4];
 #pragma unroll
     for (int i = 0; i < 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.0f;
-    float m_run[2] = {-INFINITY, -INFINITY};
+    float m_ref[2] = {-INFINITY, -INFINITY};   // exp2 offset per row (log2 units)
     float l_run[2] = {0.0f, 0.0f};
-    float sigma = FLT_MIN;
-    const float sl2 = args.sm_scale_log2;
+    float sigma = FLT_MIN;                     // running max of this tile's row scales
+    float inv_sigma = 1.0f / FLT_MIN;
+    bool failed = false;
 
     for (int b = 0; b < nblk; ++b) {
         const int s = b % kStages;
-        const bool ok = mbar_wait_bounded(&bars[s], static_cast<uint32_t>((b / kStages) & 1));
-        if (__syncthreads_or(!ok)) {
-            // A copy did not land in time: record it, drain what is still in
-            // flight (bounded as well) and leave without touching the outputs.
-            if (threadIdx.x == 0) {
-                atomicOr(args.err, MLA_ERR_PIPELINE_TIMEOUT);
-                for (int bb = b; bb < min(nblk, b + kStages); ++bb)
-                    (void)mbar_wait_bounded(&bars[bb % kStages], static_cast<uint32_t>((bb / kStages) & 1));
-            }
-            __syncthreads();
-            return;
-        }
+        const bool ok = mbar_wait_bounded(&full[s], static_cast<uint32_t>((b / kStages) & 1));
         const uint8_t* st = stages + s * kStageBytes;
         const int n_b = min(kNB, n_valid - b * kNB);
 
-        // QK^T: latent on f16 MMA, RoPE on bf16 MMA.
+        // QK^T: latent on f16 MMA (4 independent accumulators per k-step).
         float acc[4][4], accr[4][4];
 #pragma unroll
-        for (int nt = 0; nt < 4; ++nt) {
+        for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
             for (int i = 0; i < 4; ++i) acc[nt][i] = accr[nt][i] = 0.0f;
-            const uint8_t* rowp = st + (nt * 8 + g) * kRowBytes;
 #pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
-                const uint4 kv = *reinterpret_cast<const uint4*>(rowp + 128 * warp + 32 * c + 16 * hf);
-                const uint32_t kw[4] = {kv.x, kv.y, kv.z, kv.w};
+        for (int hf = 0; hf < 2; ++hf) {
+            uint4 kv[4];
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    mma_f16(acc[nt], qa[4 * hf + kk], e4m3x2_to_f16x2(kw[kk]), e4m3x2_to_f16x2(kw[kk] >> 16));
+            for (int nt = 0; nt < 4; ++nt)
+                kv[nt] = *reinterpret_cast<const uint4*>(st + (nt * 8 + g) * kRowBytes + 128 * warp + 32 * c + 16 * hf);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+#pragma unroll
+                for (int nt = 0; nt < 4; ++nt) {
+                    const uint32_t wrd = kk == 0 ? kv[nt].x : kk == 1 ? kv[nt].y : kk == 2 ? kv[nt].z : kv[nt].w;
+                    uint32_t b0, b1;
+                    e4m3x4_to_f16x2x2(wrd, b0, b1);
+                    mma_f16(acc[nt], qa[4 * hf + kk], b0, b1);
+                }
             }
-            if (with_rope) {
-                const uint2 rb = *reinterpret_cast<const uint2*>(rowp + kTailOff + 32 * warp + 8 * c);
+        }
+        if (kRopeOn) {
+#pragma unroll
+            for (int nt = 0; nt < 4; ++nt) {
+                const uint2 rb = *reinterpret_cast<const uint2*>(st + (nt * 8 + g) * kRowBytes + kTailOff + 32 * warp + 8 * c);
                 mma_bf16(accr[nt], qra, rb.x, rb.y);
             }
         }
-        // Per-row tile scale (rows past n_b were zero-filled: scale 0).
+        // Row scale of tile `warp` for the 8 columns this thread holds
+        // (rows past n_b were zero-filled: scale 0).
         float sc[4][2];
 #pragma unroll
         for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
             for (int e = 0; e < 2; ++e)
                 sc[nt][e] = *reinterpret_cast<const float*>(st + (nt * 8 + 2 * c + e) * kRowBytes + kScaleOff + 4 * warp);
-        // Reduction buffer as float4 [warp][nt][lane]: conflict-free 16-byte accesses.
-        float4* red4 = reinterpret_cast<float4*>(red);
+        float4* rbuf = red + (b & 1) * (kWarps * 4 * 32);
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt)
+            rbuf[(warp * 4 + nt) * 32 + lane] =
+                make_float4(fmaf(acc[nt][0], sc[nt][0], accr[nt][0]), fmaf(acc[nt][1], sc[nt][1], accr[nt][1]),
+                            fmaf(acc[nt][2], sc[nt][0], accr[nt][2]), fmaf(acc[nt][3], sc[nt][1], accr[nt][3]));
+        // One barrier per block for the four consumer warps; it also carries a
+        // timeout of any of them to all of them.
+        if (bar_sync_or(1, kConsumerThreads, !ok)) { failed = true; break; }
+        float sv[4][4];
 #pragma unroll
         for (int nt = 0; nt < 4; ++nt) {
-            float4 v;
-            v.x = acc[nt][0] * (sc[nt][0] * qup[0]) + accr[nt][0];
-            v.y = acc[nt][1] * (sc[nt][1] * qup[0]) + accr[nt][1];
-            v.z = acc[nt][2] * (sc[nt][0] * qup[1]) + accr[nt][2];
-            v.w = acc[nt][3] * (sc[nt][1] * qup[1]) + accr[nt][3];
-            red4[(warp * 4 + nt) * 32 + lane] = v;
-        }
-        __syncthreads();
-        float sfull[4][4];
-#pragma unroll
-        for (int nt = 0; nt < 4; ++nt) {
-            float4 a = red4[nt * 32 + lane];
+            float4 a = rbuf[nt * 32 + lane];
 #pragma unroll
             for (int w = 1; w < kWarps; ++w) {
-                const float4 bq = red4[(w * 4 + nt) * 32 + lane];
+                const float4 bq = rbuf[(w * 4 + nt) * 32 + lane];
                 a.x += bq.x; a.y += bq.y; a.z += bq.z; a.w += bq.w;
             }
-            sfull[nt][0] = a.x; sfull[nt][1] = a.y; sfull[nt][2] = a.z; sfull[nt][3] = a.w;
+            sv[nt][0] = a.x * rowf[0]; sv[nt][1] = a.y * rowf[0];
+            sv[nt][2] = a.z * rowf[1]; sv[nt][3] = a.w * rowf[1];
         }
-
-        // Online softmax in log2 units; columns past n_b are absent.
+        if (n_b < kNB) {
+#pragma unroll
+            for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    if (nt * 8 + 2 * c + (i & 1) >= n_b) sv[nt][i] = -INFINITY;
+        }
         float rmax[2] = {-INFINITY, -INFINITY};
+        float smax = 0.0f;
 #pragma unroll
         for (int nt = 0; nt < 4; ++nt) {
+            rmax[0] = fmaxf(rmax[0], fmaxf(sv[nt][0], sv[nt][1]));
+            rmax[1] = fmaxf(rmax[1], fmaxf(sv[nt][2], sv[nt][3]));
+            smax = fmaxf(smax, fmaxf(sc[nt][0], sc[nt][1]));
+        }
+        rmax[0] = quad_max(rmax[0]);
+        rmax[1] = quad_max(rmax[1]);
+        smax = quad_max(smax);
+        const bool move0 = rmax[0] > m_ref[0] + kRescaleSlack;
+        const bool move1 = rmax[1] > m_ref[1] + kRescaleSlack;
+        if (__any_sync(0xffffffffu, move0 || move1 || smax > sigma)) {
+            // Rare after the first blocks: move the exp2 offsets and/or sigma and
+            // rescale O and l accordingly.
+            const float mn0 = move0 ? rmax[0] : m_ref[0];
+            const float mn1 = move1 ? rmax[1] : m_ref[1];
+            const float a0 = ex2_approx(m_ref[0] - mn0);     // -inf -> 0
+            const float a1 = ex2_approx(m_ref[1] - mn1);
+            const float sig_new = fmaxf(sigma, smax);
+            const float rs = sigma / sig_new;
+            const float f0 = a0 * rs, f1 = a1 * rs;
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int j = nt * 8 + 2 * c + (i & 1);
-                const float v = (j < n_b) ? sfull[nt][i] * sl2 : -INFINITY;
-                sfull[nt][i] = v;
-                rmax[i >> 1] = fmaxf(rmax[i >> 1], v);
+            for (int i = 0; i < 16; ++i) {
+                o[i][0] *= f0; o[i][1] *= f0; o[i][2] *= f1; o[i][3] *= f1;
             }
-        }
-        float alpha[2], m_use[2];
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-            rmax[r] = fmaxf(rmax[r], __shfl_xor_sync(0xffffffffu, rmax[r], 1));
-            rmax[r] = fmaxf(rmax[r], __shfl_xor_sync(0xffffffffu, rmax[r], 2));
-            const float m_new = fmaxf(m_run[r], rmax[r]);
-            m_use[r] = (m_new == -INFINITY) ? 0.0f : m_new;
-            alpha[r] = exp2f(m_run[r] - m_use[r]);
-            m_run[r] = m_new;
-        }
-        float psum[2] = {0.0f, 0.0f};
-#pragma unroll
-        for (int nt = 0; nt < 4; ++nt) {
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const float p = exp2f(sfull[nt][i] - m_use[i >> 1]);
-                sfull[nt][i] = p;
-                psum[i >> 1] += p;
-            }
-        }
-        l_run[0] = l_run[0] * alpha[0] + psum[0];
-        l_run[1] = l_run[1] * alpha[1] + psum[1];
-
-        // Running max of this tile's scales keeps the f16 P operand in [0, 1].
-        const float sblk = warp_max((lane < n_b)
-            ? *reinterpret_cast<const float*>(st + lane * kRowBytes + kScaleOff + 4 * warp) : 0.0f);
-        const float sig_new = fmaxf(sigma, sblk);
-        const float rs = sigma / sig_new;
-        const float inv = 1.0f / sig_new;
-        sigma = sig_new;
-        const float f0 = alpha[0] * rs, f1 = alpha[1] * rs;
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            o[i][0] *= f0; o[i][1] *= f0; o[i][2] *= f1; o[i][3] *= f1;
+            l_run[0] *= a0;
+            l_run[1] *= a1;
+            m_ref[0] = mn0;
+            m_ref[1] = mn1;
+            sigma = sig_new;
+            inv_sigma = 1.0f / sig_new;
         }
         uint32_t pa[2][4];
 #pragma unroll
-        for (int kb = 0; kb < 2; ++kb) {
-            const int n0 = 2 * kb, n1 = 2 * kb + 1;
-            const float a0 = sc[n0][0] * inv, a1 = sc[n0][1] * inv, b0 = sc[n1][0] * inv, b1 = sc[n1][1] * inv;
-            pa[kb][0] = pack_f16x2(sfull[n0][0] * a0, sfull[n0][1] * a1);
-            pa[kb][1] = pack_f16x2(sfull[n0][2] * a0, sfull[n0][3] * a1);
-            pa[kb][2] = pack_f16x2(sfull[n1][0] * b0, sfull[n1][1] * b1);
-            pa[kb][3] = pack_f16x2(sfull[n1][2] * b0, sfull[n1][3] * b1);
+        for (int nt = 0; nt < 4; ++nt) {
+            const float p0 = ex2_approx(sv[nt][0] - m_ref[0]);
+            const float p1 = ex2_approx(sv[nt][1] - m_ref[0]);
+            const float p2 = ex2_approx(sv[nt][2] - m_ref[1]);
+            const float p3 = ex2_approx(sv[nt][3] - m_ref[1]);
+            l_run[0] += p0 + p1;
+            l_run[1] += p2 + p3;
+            const float r0 = sc[nt][0] * inv_sigma, r1 = sc[nt][1] * inv_sigma;
+            pa[nt >> 1][(nt & 1) * 2 + 0] = pack_f16x2(p0 * r0, p1 * r1);
+            pa[nt >> 1][(nt & 1) * 2 + 1] = pack_f16x2(p2 * r0, p3 * r1);
         }
 
         // PV: V rows j as K, dims of tile `warp` as N.
@@ -367,19 +379,35 @@ mla_sparse_decode_kernel(const DecodeArgs args) {
                 const uint32_t W1 = *reinterpret_cast<const uint32_t*>(vb + (j0 + 1) * kRowBytes + 32 * qd);
                 const uint32_t W2 = *reinterpret_cast<const uint32_t*>(vb + (j0 + 8) * kRowBytes + 32 * qd);
                 const uint32_t W3 = *reinterpret_cast<const uint32_t*>(vb + (j0 + 9) * kRowBytes + 32 * qd);
-                const uint32_t p01a = prmt(W0, W1, 0x5140), p01b = prmt(W0, W1, 0x7362);
-                const uint32_t p23a = prmt(W2, W3, 0x5140), p23b = prmt(W2, W3, 0x7362);
-                mma_f16(o[4 * qd + 0], pa[kb], e4m3x2_to_f16x2(p01a), e4m3x2_to_f16x2(p23a));
-                mma_f16(o[4 * qd + 1], pa[kb], e4m3x2_to_f16x2(p01a >> 16), e4m3x2_to_f16x2(p23a >> 16));
-                mma_f16(o[4 * qd + 2], pa[kb], e4m3x2_to_f16x2(p01b), e4m3x2_to_f16x2(p23b));
-                mma_f16(o[4 * qd + 3], pa[kb], e4m3x2_to_f16x2(p01b >> 16), e4m3x2_to_f16x2(p23b >> 16));
+                uint32_t b0a, b0b, b0c, b0d, b1a, b1b, b1c, b1d;
+                e4m3x4_to_f16x2x2(prmt(W0, W1, 0x5140), b0a, b0b);   // d offsets 0, 1
+                e4m3x4_to_f16x2x2(prmt(W0, W1, 0x7362), b0c, b0d);   // d offsets 2, 3
+                e4m3x4_to_f16x2x2(prmt(W2, W3, 0x5140), b1a, b1b);
+                e4m3x4_to_f16x2x2(prmt(W2, W3, 0x7362), b1c, b1d);
+                mma_f16(o[4 * qd + 0], pa[kb], b0a, b1a);
+                mma_f16(o[4 * qd + 1], pa[kb], b0b, b1b);
+                mma_f16(o[4 * qd + 2], pa[kb], b0c, b1c);
+                mma_f16(o[4 * qd + 3], pa[kb], b0d, b1d);
             }
         }
-        __syncthreads();          // stage s and the reduction buffer are free again
-        if (warp == 0 && b + kStages < nblk) issue(b + kStages);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
     }
 
-    // ---- 5. epilogue ----
+    __syncthreads();     // all 5 warps: producer done issuing, consumers done reading
+    if (failed || *issued_s < nblk) {
+        // A wait ran out: record it, let the copies already issued land (bounded)
+        // and leave without touching the outputs.
+        if (threadIdx.x == 0) {
+            atomicOr(args.err, MLA_ERR_PIPELINE_TIMEOUT);
+            const int issued = *issued_s;
+            for (int bb = max(0, issued - kStages); bb < issued; ++bb)
+                (void)mbar_wait_bounded(&full[bb % kStages], static_cast<uint32_t>((bb / kStages) & 1));
+        }
+        return;
+    }
+
+    // ---- epilogue ----
     float lt[2];
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
@@ -389,19 +417,19 @@ mla_sparse_decode_kernel(const DecodeArgs args) {
         lt[r] = l;
     }
     const float mult[2] = {lt[0] > 0.0f ? sigma / lt[0] : 0.0f, lt[1] > 0.0f ? sigma / lt[1] : 0.0f};
-    const float lse_r[2] = {lt[0] > 0.0f ? (m_run[0] + log2f(lt[0])) * kLn2 : -INFINITY,
-                            lt[1] > 0.0f ? (m_run[1] + log2f(lt[1])) * kLn2 : -INFINITY};
+    const float lse_r[2] = {lt[0] > 0.0f ? (m_ref[0] + log2f(lt[0])) * kLn2 : -INFINITY,
+                            lt[1] > 0.0f ? (m_ref[1] + log2f(lt[1])) * kLn2 : -INFINITY};
     const int hs[2] = {h_lo, h_hi};
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
         const int h = hs[r];
         if (h >= H) continue;
         const int i0 = 2 * r, i1 = 2 * r + 1;
+        const float mm = mult[r];
         if (args.nsplit == 1) {
             __nv_bfloat16* orow = args.out + (static_cast<int64_t>(t) * H + h) * kLatent + 128 * warp + 8 * c;
 #pragma unroll
             for (int qd = 0; qd < 4; ++qd) {
-                const float mm = mult[r];
                 uint4 v;
                 v.x = pack_bf16x2(o[4 * qd + 0][i0] * mm, o[4 * qd + 1][i0] * mm);
                 v.y = pack_bf16x2(o[4 * qd + 2][i0] * mm, o[4 * qd + 3][i0] * mm);
@@ -415,13 +443,10 @@ mla_sparse_decode_kernel(const DecodeArgs args) {
             float* orow = args.ws_o + prow * kLatent + 128 * warp + 8 * c;
 #pragma unroll
             for (int qd = 0; qd < 4; ++qd) {
-                const float mm = mult[r];
-                const float4 v0 = make_float4(o[4 * qd + 0][i0] * mm, o[4 * qd + 1][i0] * mm,
-                                              o[4 * qd + 2][i0] * mm, o[4 * qd + 3][i0] * mm);
-                const float4 v1 = make_float4(o[4 * qd + 0][i1] * mm, o[4 * qd + 1][i1] * mm,
-                                              o[4 * qd + 2][i1] * mm, o[4 * qd + 3][i1] * mm);
-                reinterpret_cast<float4*>(orow + 32 * qd)[0] = v0;
-                reinterpret_cast<float4*>(orow + 32 * qd)[1] = v1;
+                reinterpret_cast<float4*>(orow + 32 * qd)[0] =
+                    make_float4(o[4 * qd + 0][i0] * mm, o[4 * qd + 1][i0] * mm, o[4 * qd + 2][i0] * mm, o[4 * qd + 3][i0] * mm);
+                reinterpret_cast<float4*>(orow + 32 * qd)[1] =
+                    make_float4(o[4 * qd + 0][i1] * mm, o[4 * qd + 1][i1] * mm, o[4 * qd + 2][i1] * mm, o[4 * qd + 3][i1] * mm);
             }
             if (warp == 0 && c == 0) args.ws_lse[prow] = lse_r[r];
         }
@@ -521,7 +546,9 @@ extern "C" int mla_sparse_decode(const void* q_bf16, int T, int H, int d_qk, mla
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MLA_ECUDA;
     if (!attr_set[dev]) {
-        if (cudaFuncSetAttribute(mla_sparse_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(mla_sparse_decode_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kSmemTotal) != cudaSuccess ||
+            cudaFuncSetAttribute(mla_sparse_decode_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  kSmemTotal) != cudaSuccess)
             return MLA_ECUDA;
         attr_set[dev] = true;
@@ -543,7 +570,10 @@ extern "C" int mla_sparse_decode(const void* q_bf16, int T, int H, int d_qk, mla
     a.sm_scale_log2 = sm_scale * kLog2e;
     const dim3 grid(static_cast<unsigned>(T), static_cast<unsigned>(nsplit), static_cast<unsigned>((H + kHeads - 1) / kHeads));
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    mla_sparse_decode_kernel<<<grid, kThreads, kSmemTotal, st>>>(a);
+    if (d_qk == kLatent + kRope)
+        mla_sparse_decode_kernel<true><<<grid, kThreads, kSmemTotal, st>>>(a);
+    else
+        mla_sparse_decode_kernel<false><<<grid, kThreads, kSmemTotal, st>>>(a);
     if (cudaGetLastError() != cudaSuccess) return MLA_ECUDA;
     if (nsplit > 1) {
         mla_split_combine_kernel<<<static_cast<unsigned>(static_cast<int64_t>(T) * H), 128, 0, st>>>(
