@@ -1,85 +1,70 @@
-// mla_sparse_decode: sparse top-k MLA decode over the packed FP8 cache, on the
-// sm_100-family tensor cores (tcgen05 + tensor memory + TMA gathers).
+// mla_sparse_decode: sparse top-k MLA decode over the packed FP8 cache.
 //
-// What it computes follows the decode statement in the C header, with the
-// masking rule of sglang PR #39288 (Root cause: a -1 candidate must add nothing
-// and must not gather slot 0) and sglang PR #47013 (Motivation: masking only the
-// score does not stop a NaN row). Here an absent entry is removed before
-// anything is fetched: each CTA compacts its slice of the top-k list in shared
-// memory, so -1, slot 0 and out-of-range indices are never dereferenced.
+// What it computes follows the decode statement quoted in the C header, with
+// the masking rule of sglang PR #39288 (Root cause: a -1 candidate must add
+// nothing and must not gather slot 0) and sglang PR #47013 (Motivation: masking
+// only the score does not stop a NaN row). Here an absent entry is removed
+// before anything is fetched: each CTA compacts its slice of the top-k list in
+// shared memory, so -1, slot 0 and out-of-range indices are never dereferenced.
 //
-// One CTA per (token, split of the top-k list, group of 16 heads); 6 warps:
-//   warp 0     producer: TMA tile::gather4 of 128 present rows per block into a
-//              2-stage ring. The four 128-byte latent tiles and the RoPE tail land
-//              in 128-byte-swizzled UMMA layouts (8-row atoms), the 16-byte scale
-//              groups in a plain array. Rows past the end of the list get an
-//              out-of-range row coordinate, which TMA fills with zeros without
-//              reading memory.
-//   warp 1     MMA issuer (one thread) and tensor-memory owner.
-//   warps 2-5  compute, thread j <-> row j of the block <-> tensor-memory lane j.
-// Per 128-row block:
-//   dequant  each compute thread converts its row's 512 E4M3 codes to f16
-//            (exact) and stores them into tensor memory: the A operand of QK.
-//   QK       S^T[j, h] = sum_t scale[j, t] * (E_t[j] . q_t[h]) + rope[j] . qr[h]:
-//            f16 MMAs (M = 128 rows, N = 16 heads, A from tensor memory) into four
-//            per-tile fp32 accumulators plus a bf16 MMA for the RoPE part, so every
-//            product is exact before fp32 accumulation and the fp32 tile scales are
-//            applied per row afterwards.
-//   softmax  online, per head, in log2 units; the exp2 offset moves only when a
-//            score exceeds it by more than 2^8.
-//   PV       O^T[d, h] += sum_j E[j, d] * P~_t[j, h], P~_t = p * scale[j, t] /
-//            sigma_t * 1.75 in [0, 448] split into two E4M3 terms (hi + lo, about
-//            2^-8 relative); kind::f8f6f4 MMAs read V^T straight from the gathered
-//            E4M3 tiles (MN-major) and accumulate O^T in tensor memory.
-// Splits write a normalised partial (o, lse) to the caller's workspace; a second
-// kernel merges them in split order (deterministic: no float atomics).
+// Work decomposition: one CTA per (token, split of the top-k list, group of 16
+// heads); 4 warps; warp w owns latent tile w (dims 128w .. 128w+127) and RoPE
+// dims 16w .. 16w+15. Present rows move global -> shared with one
+// cp.async.bulk per row (656 B, or 528 B for NoPE: the tail is not read) into
+// a 4-stage ring of 32-row blocks, each stage completing on an mbarrier.
+//
+// Arithmetic per 32-row block, on tensor cores (m16n8k16, heads as M):
+//   QK  : the E4M3 latent goes to f16 exactly (cvt.f16x2.e4m3x2); q goes to f16
+//         exactly after an exponent-only per-head rescale that keeps it in f16
+//         range; the per-row, per-tile fp32 scale multiplies each warp's tile
+//         partial afterwards, so the product q.K is exact before fp32
+//         accumulation. RoPE dims run as a bf16 MMA on the stored bf16 values.
+//   softmax: the four tile partials are summed through shared memory; online
+//         max / sum in fp32 with exp2 (log2 e folded into sm_scale).
+//   PV  : p * scale_row / sigma (sigma = running max of the tile's scales, so the
+//         f16 operand stays in [0, 1]) times the exact f16 E4M3 codes; O stays
+//         in registers (16 heads x 128 dims per warp) and is rescaled with the
+//         softmax correction.
+// Splits write a normalised partial (o, lse) to the caller's workspace and a
+// second kernel merges them in split order (deterministic: no float atomics).
 #include <cfloat>
 #include <cmath>
-#include <cstring>
-#include <mutex>
 
 #include "mla_device.cuh"
-#include "mla_tcgen05.cuh"
 
 namespace {
 
 using namespace mla;
-namespace tc = mla::tc;
 
-constexpr int kBM = 128;               // rows per block: M of QK, K of PV
-constexpr int kHG = 16;                // heads per CTA: N of both MMAs
-constexpr int kListMax = 1024;         // top-k positions one CTA compacts
-constexpr int kThreads = 192;
-constexpr int kWarpsAll = kThreads / 32;
-constexpr int kComputeThreads = 128;
+constexpr int kHeads = 16;                   // heads per CTA (M of m16n8k16)
+constexpr int kWarps = 4;                    // consumer warps (one per latent tile)
+constexpr int kProducer = kWarps;            // warp index of the copy-issuing warp
+constexpr int kThreads = (kWarps + 1) * 32;
+constexpr int kConsumerThreads = kWarps * 32;
+constexpr int kNB = 32;                      // rows per block
+constexpr int kStages = 4;
+constexpr int kListMax = 2304;               // positions one CTA compacts
+constexpr int kStageBytes = kNB * kRowBytes; // 20,992
+constexpr int kSmemStages = kStages * kStageBytes;
+constexpr int kSmemList = kListMax * 4;
+constexpr int kSmemRed = 2 * kWarps * 4 * 32 * 16;   // two buffers of float4 [warp][n-tile][lane]
+constexpr int kSmemQmax = kWarps * kHeads * 4;
+constexpr int kSmemMisc = 16 + 2 * kStages * 8 + 16; // warp counts, full + empty barriers, issued count
+constexpr int kSmemTotal = kSmemStages + kSmemList + kSmemRed + kSmemQmax + kSmemMisc;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
-constexpr float kRescaleSlack = 8.0f;  // log2 units: p <= 2^8
-constexpr float kPScale = 1.75f;       // maps [0, 256] onto [0, 448]
+// The running max used as the exp2 offset is only moved when a score exceeds it
+// by more than this (log2 units): p <= 2^8 keeps the f16 P operand in range.
+constexpr float kRescaleSlack = 8.0f;
 
-// Shared memory, offsets from a 1024-byte aligned base.
-constexpr uint32_t kLatBytes = 4 * 16 * 1024;        // 4 tiles x 16 atoms of 8 rows x 128 B
-constexpr uint32_t kRopeBytes = 16 * 1024;           // 16 atoms of 8 rows x 64 bf16
-constexpr uint32_t kScaleBytes = 32 * 128;           // 32 groups of 4 rows x 16 B
-constexpr uint32_t kStageBytes = kLatBytes + kRopeBytes + kScaleBytes;   // 86,016
-constexpr uint32_t kOffQ = 2 * kStageBytes;          // f16 q latent, K-major 128-B swizzle
-constexpr uint32_t kOffQR = kOffQ + 16384;           // bf16 q RoPE
-constexpr uint32_t kOffP = kOffQR + 2048;            // 2 x P~ [tile][term][16 core matrices of 128 B]
-constexpr uint32_t kPBytes = 4 * 2 * 16 * 128;
-constexpr uint32_t kOffList = kOffP + 2 * kPBytes;
-constexpr uint32_t kOffRed = kOffList + kListMax * 4;   // [4 warps][32] floats
-constexpr uint32_t kOffBar = kOffRed + 512;
-constexpr uint32_t kSmemUsed = kOffBar + 192;
-constexpr uint32_t kSmemAlloc = kSmemUsed + 1024;    // slack to align the base to 1024 B
-
-// Tensor-memory columns (one CTA per SM allocates all 512).
-constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColA = 0;     // 256: f16 latent rows of the block
-constexpr uint32_t kColS = 256;   // 80: S^T per tile (4 x 16) + RoPE (16)
-constexpr uint32_t kColO = 336;   // 64: O^T per tile (4 x 16)
+__device__ __forceinline__ float quad_max(float v) {
+    v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 1));
+    return fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 2));
+}
 
 struct DecodeArgs {
     const __nv_bfloat16* q;
+    const uint8_t* cache;
     const int32_t* topk;
     __nv_bfloat16* out;
     float* lse;
@@ -87,109 +72,56 @@ struct DecodeArgs {
     float* ws_lse;    // [T, nsplit, H]
     int* err;
     int64_t num_slots;
-    int oob_row;      // a row coordinate past the tensor map (zero fill)
     int T, H, d_qk, W, nsplit, split_len;
     float sm_scale_log2;   // sm_scale * log2(e)
 };
 
-// Bounded wait that also gives up when another role has already given up.
-__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const long long t0 = clock64();
-    for (;;) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if (*abort_flag) return false;
-        if (clock64() - t0 > kWaitCycles) {
-            *abort_flag = 1;
-            return false;
-        }
-    }
-}
-
-__device__ __forceinline__ float warp_max(float v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-    return v;
-}
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    return v;
-}
-
-// Two E4M3 codes of (x0, x1): low byte = x0. Round to nearest even, saturating.
-__device__ __forceinline__ uint32_t e4m3x2(float x0, float x1) {
-    return static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(make_float2(x0, x1), __NV_SATFINITE, __NV_E4M3));
-}
-// hi + lo E4M3 split of a pair: hi = e4m3(x), lo = e4m3(x - hi).
-__device__ __forceinline__ void split2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
-    hi = e4m3x2(x0, x1);
-    uint32_t hf, unused;
-    e4m3x4_to_f16x2x2(hi, hf, unused);
-    const float2 hv = __half22float2(*reinterpret_cast<const __half2*>(&hf));
-    lo = e4m3x2(x0 - hv.x, x1 - hv.y);
-}
-
 template <bool kRopeOn>
-__global__ void __launch_bounds__(kThreads, 1)
-mla_sparse_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_row, const __grid_constant__ CUtensorMap tm_scale,
-                            const DecodeArgs args) {
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const uint32_t sbase = smem_u32(smem);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
-    uint64_t* full = bars;          // [2] stage landed (TMA bytes)
-    uint64_t* empty = bars + 2;     // [2] PV of the stage's block complete
-    uint64_t* a_ready = bars + 4;   // dequant written to tensor memory (4 warps)
-    uint64_t* s_full = bars + 5;    // QK complete
-    uint64_t* p_ready = bars + 6;   // [2] P~ written (4 warps)
-    uint64_t* drain = bars + 8;     // all MMAs complete (end of kernel)
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 9);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-    int* issued_s = reinterpret_cast<int*>(tmem_slot + 2);
-    int* wcount = reinterpret_cast<int*>(tmem_slot + 3);          // [6]
-    int* list = reinterpret_cast<int*>(smem + kOffList);
-    float* red = reinterpret_cast<float*>(smem + kOffRed);
+__global__ void __launch_bounds__(kThreads, 2)
+mla_sparse_decode_kernel(const DecodeArgs args) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint8_t* stages = smem;
+    int* list = reinterpret_cast<int*>(smem + kSmemStages);
+    float4* red = reinterpret_cast<float4*>(smem + kSmemStages + kSmemList);
+    float* qmax_s = reinterpret_cast<float*>(smem + kSmemStages + kSmemList + kSmemRed);
+    int* wcount = reinterpret_cast<int*>(smem + kSmemStages + kSmemList + kSmemRed + kSmemQmax);
+    uint64_t* full = reinterpret_cast<uint64_t*>(wcount + 4);
+    uint64_t* empty = full + kStages;
+    int* issued_s = reinterpret_cast<int*>(empty + kStages);
 
-    const int warp = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
     const int t = blockIdx.x;
     const int split = blockIdx.y;
     const int hg = blockIdx.z;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
     const int H = args.H;
+    constexpr uint32_t kRowRead = kRopeOn ? kRowBytes : kNopeReadBytes;
 
     if (threadIdx.x == 0) {
-        mbar_init(&full[0], 1); mbar_init(&full[1], 1);
-        mbar_init(&empty[0], 1); mbar_init(&empty[1], 1);
-        mbar_init(a_ready, 4); mbar_init(s_full, 1);
-        mbar_init(&p_ready[0], 4); mbar_init(&p_ready[1], 4);
-        mbar_init(drain, 1);
-        *abort_flag = 0;
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kWarps);
+        }
         *issued_s = 0;
         fence_mbar_init();
     }
-    if (warp == 1) {
-        tc::tmem_alloc(tmem_slot, kTmemCols);
-        tc::tmem_relinquish();
-        tc::fence_before_sync();
-    }
 
-    // ---- compact the present entries of this split's positions (all warps) ----
+    // ---- 1. compact the present entries of this split's positions (all warps) ----
     const int p0 = split * args.split_len;
     const int p1 = min(args.W, p0 + args.split_len);
     const int32_t* trow = args.topk + static_cast<int64_t>(t) * args.W;
     int n_valid = 0;
-    for (int base = p0; base < p1; base += kThreads) {
+    for (int base = p0; base < p1; base += kConsumerThreads) {
         const int pos = base + threadIdx.x;
-        const int idx = (pos < p1) ? __ldg(trow + pos) : -1;
+        const int idx = (warp < kWarps && pos < p1) ? __ldg(trow + pos) : -1;
         const bool valid = idx > 0 && static_cast<int64_t>(idx) < args.num_slots;
         if (idx > 0 && !valid) atomicOr(args.err, MLA_ERR_DECODE_INDEX_RANGE);
         const unsigned m = __ballot_sync(0xffffffffu, valid);
-        if (lane == 0) wcount[warp] = __popc(m);
+        if (lane == 0 && warp < kWarps) wcount[warp] = __popc(m);
         __syncthreads();
         int off = n_valid, total = 0;
 #pragma unroll
-        for (int w = 0; w < kWarpsAll; ++w) {
+        for (int w = 0; w < kWarps; ++w) {
             const int cw = wcount[w];
             off += (w < warp) ? cw : 0;
             total += cw;
@@ -198,389 +130,326 @@ mla_sparse_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_row, const __
         n_valid += total;
         __syncthreads();
     }
-    __syncthreads();
-    tc::fence_after_sync();
-    const uint32_t tmem = *tmem_slot;
-    const int nblk = (n_valid + kBM - 1) / kBM;
+    const int nblk = (n_valid + kNB - 1) / kNB;
 
-    if (warp == 0) {
-        // ================= producer =================
+    if (warp == kProducer) {
+        // ---- producer: lane j copies row j of each block into the stage ring ----
         int b = 0;
         for (; b < nblk; ++b) {
-            const int s = b & 1;
-            if (b >= 2 && !wait_or_abort(&empty[s], static_cast<uint32_t>(((b >> 1) - 1) & 1), abort_flag)) break;
-            uint8_t* st = smem + s * kStageBytes;
-            if (lane == 0) mbar_arrive_expect_tx(&full[s], kBM * ((kRopeOn ? 640u : 512u) + 16u));
+            const int s = b % kStages;
+            if (b >= kStages && !mbar_wait_bounded(&empty[s], static_cast<uint32_t>(((b / kStages) - 1) & 1))) {
+                if (lane == 0) atomicOr(args.err, MLA_ERR_PIPELINE_TIMEOUT);
+                break;
+            }
+            uint8_t* dst = stages + s * kStageBytes;
+            const int n_b = min(kNB, n_valid - b * kNB);
+            if (n_b < kNB) {
+                // Rows past the end of the list load nothing: zero them so the
+                // block's arithmetic sees finite zeros (E4M3 0, scale 0.0).
+                if (lane >= n_b) {
+                    uint4* z = reinterpret_cast<uint4*>(dst + lane * kRowBytes);
+                    for (int k = 0; k < kRowBytes / 16; ++k) z[k] = make_uint4(0u, 0u, 0u, 0u);
+                }
+                fence_proxy_async_smem();
+            }
             __syncwarp();
-            // lane g gathers rows 4g .. 4g+3 of the block: half an 8-row atom
-            const int r0 = b * kBM + 4 * lane;
-            int y[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) y[i] = (r0 + i < n_valid) ? list[r0 + i] : args.oob_row;
-            uint8_t* dst = st + (lane >> 1) * 1024 + (lane & 1) * 512;
-#pragma unroll
-            for (int tt = 0; tt < 4; ++tt)
-                tc::tma_gather4(dst + tt * 16384, &tm_row, 128 * tt, y[0], y[1], y[2], y[3], &full[s]);
-            if (kRopeOn)
-                tc::tma_gather4(dst + kLatBytes, &tm_row, kTailOff, y[0], y[1], y[2], y[3], &full[s]);
-            tc::tma_gather4(st + kLatBytes + kRopeBytes + lane * 128, &tm_scale, kScaleOff, y[0], y[1], y[2], y[3],
-                            &full[s]);
+            if (lane == 0) mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(n_b) * kRowRead);
+            __syncwarp();
+            if (lane < n_b)
+                bulk_g2s(dst + lane * kRowBytes,
+                         args.cache + static_cast<int64_t>(list[b * kNB + lane]) * kRowBytes, kRowRead, &full[s]);
         }
         if (lane == 0) *issued_s = b;
-    } else if (warp == 1) {
-        // ================= MMA issuer =================
-        if (lane == 0) {
-            constexpr uint32_t id_qk = tc::instr_desc(tc::kF16, tc::kF16, false, false, 128, kHG);
-            constexpr uint32_t id_qr = tc::instr_desc(tc::kBF16, tc::kBF16, false, false, 128, kHG);
-            constexpr uint32_t id_pv = tc::instr_desc(tc::kE4M3, tc::kE4M3, true, true, 128, kHG);
-            for (int b = 0; b < nblk; ++b) {
-                const int s = b & 1;
-                if (!wait_or_abort(a_ready, static_cast<uint32_t>(b & 1), abort_flag)) break;
-                tc::fence_after_sync();
-                // QK^T latent: A = f16 rows in tensor memory, B = q (K-major, 128-B swizzle)
-#pragma unroll 4
-                for (int ks = 0; ks < 32; ++ks) {
-                    const uint64_t bd = tc::smem_desc(sbase + kOffQ + (ks >> 2) * 2048 + (ks & 3) * 32, 16, 1024, tc::kSw128);
-                    tc::mma_f16_ts(tmem + kColS + 16 * (ks >> 3), tmem + kColA + 8 * ks, bd, id_qk,
-                                   (ks & 7) != 0 ? 1u : 0u);
-                }
-                if (kRopeOn) {
-                    const uint32_t rb = sbase + s * kStageBytes + kLatBytes;
-#pragma unroll
-                    for (int kr = 0; kr < 4; ++kr) {
-                        const uint64_t ad = tc::smem_desc(rb + kr * 32, 16, 1024, tc::kSw128);
-                        const uint64_t bd = tc::smem_desc(sbase + kOffQR + kr * 32, 16, 1024, tc::kSw128);
-                        tc::mma_f16_ss(tmem + kColS + 64, ad, bd, id_qr, kr != 0 ? 1u : 0u);
-                    }
-                }
-                tc::commit(s_full);
-                if (!wait_or_abort(&p_ready[b & 1], static_cast<uint32_t>((b >> 1) & 1), abort_flag)) break;
-                tc::fence_after_sync();
-                // PV: A = V^T (E4M3, MN-major, the gathered tiles), B = P~ (E4M3, MN-major)
-                const uint32_t lat = sbase + s * kStageBytes;
-                const uint32_t pb = sbase + kOffP + (b & 1) * kPBytes;
-#pragma unroll
-                for (int tt = 0; tt < 4; ++tt) {
-#pragma unroll
-                    for (int term = 0; term < 2; ++term) {
-#pragma unroll
-                        for (int ke = 0; ke < 4; ++ke) {
-                            const uint64_t ad = tc::smem_desc(lat + tt * 16384 + ke * 4096, 16384, 1024, tc::kSw128);
-                            const uint64_t bd = tc::smem_desc(pb + (tt * 2 + term) * 2048 + ke * 512, 128, 2048, tc::kSwNone);
-                            tc::mma_f8_ss(tmem + kColO + 16 * tt, ad, bd, id_pv, (b | term | ke) != 0 ? 1u : 0u);
-                        }
-                    }
-                }
-                tc::commit(&empty[s]);
-            }
-            // Let every MMA this thread issued finish before the CTA tears down.
-            tc::commit(drain);
-            (void)mbar_wait_bounded(drain, 0);
-        }
-        __syncwarp();
-    } else {
-        // ================= compute warps =================
-        const int qd = warp & 3;                     // tensor-memory lane quarter of this warp
-        const int j = 32 * qd + lane;                // row of the block / tensor-memory lane
-        const int ct = threadIdx.x - 64;             // 0 .. 127
-        const uint32_t lane_base = static_cast<uint32_t>(32 * qd) << 16;
-        const int64_t qrow0 = static_cast<int64_t>(t) * H + hg * kHG;
+        __syncthreads();     // matches the consumers' final barrier
+        return;
+    }
 
-        // ---- q: per-head exponent shift into f16 range, then the UMMA layouts ----
-        {
-            const int h = ct >> 3, part = ct & 7;
-            float mx = 0.0f;
-            if (hg * kHG + h < H) {
-                const __nv_bfloat16* qh = args.q + (qrow0 + h) * args.d_qk;
-                const uint8_t* pl = reinterpret_cast<const uint8_t*>(qh + 64 * part);
+    // ---- consumers: q fragments ----
+    const int g = lane >> 2;
+    const int c = lane & 3;
+    const int h_lo = hg * kHeads + g;
+    const int h_hi = h_lo + 8;
+    uint32_t qraw[2][16];
+    uint32_t qr[2][2];
+    float qm[2];
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const uint4 v = ld_nc_v4(pl + 16 * k);
-                    const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+    for (int r = 0; r < 2; ++r) {
+        const int h = r ? h_hi : h_lo;
+        qm[r] = 0.0f;
+        qr[r][0] = qr[r][1] = 0u;
+        if (h < H) {
+            const __nv_bfloat16* qh = args.q + (static_cast<int64_t>(t) * H + h) * args.d_qk;
+            const uint8_t* p = reinterpret_cast<const uint8_t*>(qh + 128 * warp + 32 * c);
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) mx = fmaxf(mx, fmaxf(fabsf(bf16lo(wv[i])), fabsf(bf16hi(wv[i]))));
-                }
-                if (kRopeOn) {
-                    const uint4 v = ld_nc_v4(qh + kLatent + 8 * part);
-                    const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+            for (int k = 0; k < 4; ++k) {
+                const uint4 v = ld_nc_v4(p + 16 * k);
+                qraw[r][4 * k + 0] = v.x; qraw[r][4 * k + 1] = v.y;
+                qraw[r][4 * k + 2] = v.z; qraw[r][4 * k + 3] = v.w;
+            }
+            if (kRopeOn) {
+                const uint2 v = *reinterpret_cast<const uint2*>(qh + kLatent + 16 * warp + 4 * c);
+                qr[r][0] = v.x; qr[r][1] = v.y;
+            }
+        } else {
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) mx = fmaxf(mx, fmaxf(fabsf(bf16lo(wv[i])), fabsf(bf16hi(wv[i]))));
+            for (int k = 0; k < 16; ++k) qraw[r][k] = 0u;
+        }
+#pragma unroll
+        for (int k = 0; k < 16; ++k) qm[r] = fmaxf(qm[r], fmaxf(fabsf(bf16lo(qraw[r][k])), fabsf(bf16hi(qraw[r][k]))));
+#pragma unroll
+        for (int k = 0; k < 2; ++k) qm[r] = fmaxf(qm[r], fmaxf(fabsf(bf16lo(qr[r][k])), fabsf(bf16hi(qr[r][k]))));
+        qm[r] = quad_max(qm[r]);
+    }
+    if (c == 0) {
+        qmax_s[warp * kHeads + g] = qm[0];
+        qmax_s[warp * kHeads + g + 8] = qm[1];
+    }
+    bar_sync_or(1, kConsumerThreads, false);
+    // Exponent-only rescale so that |q| < 2^15 in f16 (exact in f16's normal
+    // range); the same power of two scales the RoPE part, and is undone on the
+    // scores through the per-row softmax factor.
+    float qdown[2], rowf[2];
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+        float mx = 0.0f;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) mx = fmaxf(mx, qmax_s[w * kHeads + g + 8 * r]);
+        int e = 0;
+        frexpf(mx, &e);                              // mx < 2^e
+        const int k = (e > 15) ? (e - 15) : 0;
+        qdown[r] = ldexpf(1.0f, -k);
+        rowf[r] = args.sm_scale_log2 * ldexpf(1.0f, k);
+    }
+    uint32_t qa[8][4];
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+            const int wi = 8 * hf + 2 * kk;
+            qa[4 * hf + kk][0] = pack_f16x2(bf16lo(qraw[0][wi]) * qdown[0], bf16hi(qraw[0][wi]) * qdown[0]);
+            qa[4 * hf + kk][1] = pack_f16x2(bf16lo(qraw[1][wi]) * qdown[1], bf16hi(qraw[1][wi]) * qdown[1]);
+            qa[4 * hf + kk][2] = pack_f16x2(bf16lo(qraw[0][wi + 1]) * qdown[0], bf16hi(qraw[0][wi + 1]) * qdown[0]);
+            qa[4 * hf + kk][3] = pack_f16x2(bf16lo(qraw[1][wi + 1]) * qdown[1], bf16hi(qraw[1][wi + 1]) * qdown[1]);
+        }
+    }
+    uint32_t qra[4];
+    qra[0] = pack_bf16x2(bf16lo(qr[0][0]) * qdown[0], bf16hi(qr[0][0]) * qdown[0]);
+    qra[1] = pack_bf16x2(bf16lo(qr[1][0]) * qdown[1], bf16hi(qr[1][0]) * qdown[1]);
+    qra[2] = pack_bf16x2(bf16lo(qr[0][1]) * qdown[0], bf16hi(qr[0][1]) * qdown[0]);
+    qra[3] = pack_bf16x2(bf16lo(qr[1][1]) * qdown[1], bf16hi(qr[1][1]) * qdown[1]);
+
+    // ---- consumers: main loop ----
+    float o[16][4];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.0f;
+    float m_ref[2] = {-INFINITY, -INFINITY};   // exp2 offset per row (log2 units)
+    float l_run[2] = {0.0f, 0.0f};
+    float sigma = FLT_MIN;                     // running max of this tile's row scales
+    float inv_sigma = 1.0f / FLT_MIN;
+    bool failed = false;
+
+    for (int b = 0; b < nblk; ++b) {
+        const int s = b % kStages;
+        const bool ok = mbar_wait_bounded(&full[s], static_cast<uint32_t>((b / kStages) & 1));
+        const uint8_t* st = stages + s * kStageBytes;
+        const int n_b = min(kNB, n_valid - b * kNB);
+
+        // QK^T: latent on f16 MMA (4 independent accumulators per k-step).
+        float acc[4][4], accr[4][4];
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) acc[nt][i] = accr[nt][i] = 0.0f;
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+            uint4 kv[4];
+#pragma unroll
+            for (int nt = 0; nt < 4; ++nt)
+                kv[nt] = *reinterpret_cast<const uint4*>(st + (nt * 8 + g) * kRowBytes + 128 * warp + 32 * c + 16 * hf);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+#pragma unroll
+                for (int nt = 0; nt < 4; ++nt) {
+                    const uint32_t wrd = kk == 0 ? kv[nt].x : kk == 1 ? kv[nt].y : kk == 2 ? kv[nt].z : kv[nt].w;
+                    uint32_t b0, b1;
+                    e4m3x4_to_f16x2x2(wrd, b0, b1);
+                    mma_f16(acc[nt], qa[4 * hf + kk], b0, b1);
                 }
             }
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-            if (part == 0) red[h] = mx;
-        }
-        bar_sync_or(1, kComputeThreads, false);
-        float rowf[kHG];
-#pragma unroll
-        for (int h = 0; h < kHG; ++h) {
-            int e = 0;
-            frexpf(red[h], &e);                              // max|q_h| < 2^e
-            rowf[h] = args.sm_scale_log2 * ldexpf(1.0f, (e > 15) ? (e - 15) : 0);
-        }
-#pragma unroll
-        for (int it = 0; it < 8; ++it) {
-            const int k = ct + kComputeThreads * it;         // 16 heads x 64 chunks of 8 dims
-            const int h = k >> 6, cc = k & 63;
-            int e = 0;
-            frexpf(red[h], &e);
-            const float down = ldexpf(1.0f, (e > 15) ? (15 - e) : 0);
-            uint4 v = make_uint4(0u, 0u, 0u, 0u);
-            if (hg * kHG + h < H) v = ld_nc_v4(args.q + (qrow0 + h) * args.d_qk + 8 * cc);
-            const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
-            uint4 o;
-            o.x = pack_f16x2(bf16lo(wv[0]) * down, bf16hi(wv[0]) * down);
-            o.y = pack_f16x2(bf16lo(wv[1]) * down, bf16hi(wv[1]) * down);
-            o.z = pack_f16x2(bf16lo(wv[2]) * down, bf16hi(wv[2]) * down);
-            o.w = pack_f16x2(bf16lo(wv[3]) * down, bf16hi(wv[3]) * down);
-            const int c64 = cc >> 3, u = cc & 7, r = h & 7;
-            *reinterpret_cast<uint4*>(smem + kOffQ + (c64 * 2 + (h >> 3)) * 1024 + r * 128 + ((u ^ r) << 4)) = o;
         }
         if (kRopeOn) {
-            const int h = ct >> 3, u = ct & 7, r = h & 7;
-            int e = 0;
-            frexpf(red[h], &e);
-            const float down = ldexpf(1.0f, (e > 15) ? (15 - e) : 0);
-            uint4 v = make_uint4(0u, 0u, 0u, 0u);
-            if (hg * kHG + h < H) v = ld_nc_v4(args.q + (qrow0 + h) * args.d_qk + kLatent + 8 * u);
-            const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
-            uint4 o;
-            o.x = pack_bf16x2(bf16lo(wv[0]) * down, bf16hi(wv[0]) * down);
-            o.y = pack_bf16x2(bf16lo(wv[1]) * down, bf16hi(wv[1]) * down);
-            o.z = pack_bf16x2(bf16lo(wv[2]) * down, bf16hi(wv[2]) * down);
-            o.w = pack_bf16x2(bf16lo(wv[3]) * down, bf16hi(wv[3]) * down);
-            *reinterpret_cast<uint4*>(smem + kOffQR + (h >> 3) * 1024 + r * 128 + ((u ^ r) << 4)) = o;
+#pragma unroll
+            for (int nt = 0; nt < 4; ++nt) {
+                const uint2 rb = *reinterpret_cast<const uint2*>(st + (nt * 8 + g) * kRowBytes + kTailOff + 32 * warp + 8 * c);
+                mma_bf16(accr[nt], qra, rb.x, rb.y);
+            }
         }
-        fence_proxy_async_smem();
-        bar_sync_or(1, kComputeThreads, false);      // red[] reads done before its reuse
-
-        float m_ref[kHG], l_part[kHG];
+        // Row scale of tile `warp` for the 8 columns this thread holds
+        // (rows past n_b were zero-filled: scale 0).
+        float sc[4][2];
 #pragma unroll
-        for (int h = 0; h < kHG; ++h) { m_ref[h] = -INFINITY; l_part[h] = 0.0f; }
-        float sigma[4] = {FLT_MIN, FLT_MIN, FLT_MIN, FLT_MIN};
-        float inv_sigma[4] = {1.0f / FLT_MIN, 1.0f / FLT_MIN, 1.0f / FLT_MIN, 1.0f / FLT_MIN};
-        bool ok = true;
-
-        for (int b = 0; b < nblk; ++b) {
-            const int s = b & 1;
-            const uint8_t* st = smem + s * kStageBytes;
-            // ---- dequant: this row's E4M3 codes -> f16 -> tensor memory ----
-            // Every failure decision is voted across the four warps, so they always
-            // take the same path through the named barrier.
-            bool okl = wait_or_abort(&full[s], static_cast<uint32_t>((b >> 1) & 1), abort_flag);
-            if (bar_sync_or(1, kComputeThreads, !okl)) { ok = false; break; }
-            {
-                const uint8_t* rowp = st + (j >> 3) * 1024 + (j & 7) * 128;
-                const int r = j & 7;
+        for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
-                for (int tt = 0; tt < 4; ++tt) {
+            for (int e = 0; e < 2; ++e)
+                sc[nt][e] = *reinterpret_cast<const float*>(st + (nt * 8 + 2 * c + e) * kRowBytes + kScaleOff + 4 * warp);
+        float4* rbuf = red + (b & 1) * (kWarps * 4 * 32);
 #pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4) {          // 16 columns = 32 dims = 2 chunks
-                        uint32_t w[16];
+        for (int nt = 0; nt < 4; ++nt)
+            rbuf[(warp * 4 + nt) * 32 + lane] =
+                make_float4(fmaf(acc[nt][0], sc[nt][0], accr[nt][0]), fmaf(acc[nt][1], sc[nt][1], accr[nt][1]),
+                            fmaf(acc[nt][2], sc[nt][0], accr[nt][2]), fmaf(acc[nt][3], sc[nt][1], accr[nt][3]));
+        // One barrier per block for the four consumer warps; it also carries a
+        // timeout of any of them to all of them.
+        if (bar_sync_or(1, kConsumerThreads, !ok)) { failed = true; break; }
+        float sv[4][4];
 #pragma unroll
-                        for (int uu = 0; uu < 2; ++uu) {
-                            const int u = 2 * q4 + uu;
-                            const uint4 v = *reinterpret_cast<const uint4*>(rowp + tt * 16384 + ((u ^ r) << 4));
-                            e4m3x4_to_f16x2x2(v.x, w[8 * uu + 0], w[8 * uu + 1]);
-                            e4m3x4_to_f16x2x2(v.y, w[8 * uu + 2], w[8 * uu + 3]);
-                            e4m3x4_to_f16x2x2(v.z, w[8 * uu + 4], w[8 * uu + 5]);
-                            e4m3x4_to_f16x2x2(v.w, w[8 * uu + 6], w[8 * uu + 7]);
-                        }
-                        tc::tmem_st16(tmem + lane_base + kColA + 64 * tt + 16 * q4, w);
-                    }
-                }
+        for (int nt = 0; nt < 4; ++nt) {
+            float4 a = rbuf[nt * 32 + lane];
+#pragma unroll
+            for (int w = 1; w < kWarps; ++w) {
+                const float4 bq = rbuf[(w * 4 + nt) * 32 + lane];
+                a.x += bq.x; a.y += bq.y; a.z += bq.z; a.w += bq.w;
             }
-            tc::wait_st();
-            tc::fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(a_ready);
-
-            // ---- softmax ----
-            okl = wait_or_abort(s_full, static_cast<uint32_t>(b & 1), abort_flag);
-            if (bar_sync_or(1, kComputeThreads, !okl)) { ok = false; break; }
-            tc::fence_after_sync();
-            const float4 scv = *reinterpret_cast<const float4*>(st + kLatBytes + kRopeBytes + (j >> 2) * 128 + (j & 3) * 16);
-            const float sc[4] = {scv.x, scv.y, scv.z, scv.w};
-            float sv[kHG];
-            {
-                uint32_t acc[16];
+            sv[nt][0] = a.x * rowf[0]; sv[nt][1] = a.y * rowf[0];
+            sv[nt][2] = a.z * rowf[1]; sv[nt][3] = a.w * rowf[1];
+        }
+        if (n_b < kNB) {
 #pragma unroll
-                for (int h = 0; h < kHG; ++h) sv[h] = 0.0f;
-                if (kRopeOn) {
-                    tc::tmem_ld16(tmem + lane_base + kColS + 64, acc);
-                    tc::wait_ld();
+            for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
-                    for (int h = 0; h < kHG; ++h) sv[h] = __uint_as_float(acc[h]);
-                }
+                for (int i = 0; i < 4; ++i)
+                    if (nt * 8 + 2 * c + (i & 1) >= n_b) sv[nt][i] = -INFINITY;
+        }
+        float rmax[2] = {-INFINITY, -INFINITY};
+        float smax = 0.0f;
 #pragma unroll
-                for (int tt = 0; tt < 4; ++tt) {
-                    tc::tmem_ld16(tmem + lane_base + kColS + 16 * tt, acc);
-                    tc::wait_ld();
+        for (int nt = 0; nt < 4; ++nt) {
+            rmax[0] = fmaxf(rmax[0], fmaxf(sv[nt][0], sv[nt][1]));
+            rmax[1] = fmaxf(rmax[1], fmaxf(sv[nt][2], sv[nt][3]));
+            smax = fmaxf(smax, fmaxf(sc[nt][0], sc[nt][1]));
+        }
+        rmax[0] = quad_max(rmax[0]);
+        rmax[1] = quad_max(rmax[1]);
+        smax = quad_max(smax);
+        const bool move0 = rmax[0] > m_ref[0] + kRescaleSlack;
+        const bool move1 = rmax[1] > m_ref[1] + kRescaleSlack;
+        if (__any_sync(0xffffffffu, move0 || move1 || smax > sigma)) {
+            // Rare after the first blocks: move the exp2 offsets and/or sigma and
+            // rescale O and l accordingly.
+            const float mn0 = move0 ? rmax[0] : m_ref[0];
+            const float mn1 = move1 ? rmax[1] : m_ref[1];
+            const float a0 = ex2_approx(m_ref[0] - mn0);     // -inf -> 0
+            const float a1 = ex2_approx(m_ref[1] - mn1);
+            const float sig_new = fmaxf(sigma, smax);
+            const float rs = sigma / sig_new;
+            const float f0 = a0 * rs, f1 = a1 * rs;
 #pragma unroll
-                    for (int h = 0; h < kHG; ++h) sv[h] = fmaf(sc[tt], __uint_as_float(acc[h]), sv[h]);
-                }
+            for (int i = 0; i < 16; ++i) {
+                o[i][0] *= f0; o[i][1] *= f0; o[i][2] *= f1; o[i][3] *= f1;
             }
-            const bool present = b * kBM + j < n_valid;
-            bool need = false;
+            l_run[0] *= a0;
+            l_run[1] *= a1;
+            m_ref[0] = mn0;
+            m_ref[1] = mn1;
+            sigma = sig_new;
+            inv_sigma = 1.0f / sig_new;
+        }
+        uint32_t pa[2][4];
 #pragma unroll
-            for (int h = 0; h < kHG; ++h) {
-                sv[h] = present ? sv[h] * rowf[h] : -INFINITY;
-                need |= sv[h] > m_ref[h] + kRescaleSlack;
-            }
-#pragma unroll
-            for (int tt = 0; tt < 4; ++tt) need |= sc[tt] > sigma[tt];
-            tc::fence_before_sync();
-            if (bar_sync_or(1, kComputeThreads, need)) {
-                // Rare after the first blocks: new per-head offsets and per-tile sigma.
-                float* rw = red + qd * 32;
-#pragma unroll
-                for (int h = 0; h < kHG; ++h) {
-                    const float mh = warp_max(sv[h]);
-                    if (lane == 0) rw[h] = mh;
-                }
-#pragma unroll
-                for (int tt = 0; tt < 4; ++tt) {
-                    const float sm = warp_max(sc[tt]);
-                    if (lane == 0) rw[16 + tt] = sm;
-                }
-                bar_sync_or(1, kComputeThreads, false);
-                float alpha[kHG], rs[4];
-#pragma unroll
-                for (int h = 0; h < kHG; ++h) {
-                    const float bm = fmaxf(fmaxf(red[h], red[32 + h]), fmaxf(red[64 + h], red[96 + h]));
-                    const float mn = (bm > m_ref[h] + kRescaleSlack) ? bm : m_ref[h];
-                    alpha[h] = ex2_approx(m_ref[h] - mn);     // -inf -> 0
-                    m_ref[h] = mn;
-                    l_part[h] *= alpha[h];
-                }
-#pragma unroll
-                for (int tt = 0; tt < 4; ++tt) {
-                    const float bs = fmaxf(fmaxf(red[16 + tt], red[48 + tt]), fmaxf(red[80 + tt], red[112 + tt]));
-                    const float sn = fmaxf(sigma[tt], bs);
-                    rs[tt] = sigma[tt] / sn;
-                    sigma[tt] = sn;
-                    inv_sigma[tt] = 1.0f / sn;
-                }
-                if (b > 0) {
-                    // O^T is rescaled in tensor memory once PV of the previous block is done.
-                    okl = wait_or_abort(&empty[(b - 1) & 1], static_cast<uint32_t>(((b - 1) >> 1) & 1), abort_flag);
-                    if (bar_sync_or(1, kComputeThreads, !okl)) {
-                        ok = false;
-                    } else {
-                        tc::fence_after_sync();
-#pragma unroll
-                        for (int tt = 0; tt < 4; ++tt) {
-                            uint32_t ov[16];
-                            tc::tmem_ld16(tmem + lane_base + kColO + 16 * tt, ov);
-                            tc::wait_ld();
-#pragma unroll
-                            for (int h = 0; h < kHG; ++h)
-                                ov[h] = __float_as_uint(__uint_as_float(ov[h]) * (alpha[h] * rs[tt]));
-                            tc::tmem_st16(tmem + lane_base + kColO + 16 * tt, ov);
-                        }
-                        tc::wait_st();
-                    }
-                }
-                bar_sync_or(1, kComputeThreads, false);   // red[] free again
-                if (!ok) break;
-            }
-            // ---- P~ = p * scale / sigma * 1.75 as E4M3 hi + lo, MN-major core matrices ----
-            {
-                float p[kHG];
-#pragma unroll
-                for (int h = 0; h < kHG; ++h) {
-                    p[h] = ex2_approx(sv[h] - m_ref[h]);
-                    l_part[h] += p[h];
-                }
-                uint8_t* pbuf = smem + kOffP + (b & 1) * kPBytes + (j >> 3) * 128 + (j & 7) * 16;
-#pragma unroll
-                for (int tt = 0; tt < 4; ++tt) {
-                    const float rt = sc[tt] * inv_sigma[tt] * kPScale;
-                    uint32_t hi[8], lo[8];
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) split2(p[2 * k] * rt, p[2 * k + 1] * rt, hi[k], lo[k]);
-                    *reinterpret_cast<uint4*>(pbuf + (tt * 2 + 0) * 2048) =
-                        make_uint4(hi[0] | (hi[1] << 16), hi[2] | (hi[3] << 16), hi[4] | (hi[5] << 16), hi[6] | (hi[7] << 16));
-                    *reinterpret_cast<uint4*>(pbuf + (tt * 2 + 1) * 2048) =
-                        make_uint4(lo[0] | (lo[1] << 16), lo[2] | (lo[3] << 16), lo[4] | (lo[5] << 16), lo[6] | (lo[7] << 16));
-                }
-            }
-            fence_proxy_async_smem();
-            tc::fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&p_ready[b & 1]);
+        for (int nt = 0; nt < 4; ++nt) {
+            const float p0 = ex2_approx(sv[nt][0] - m_ref[0]);
+            const float p1 = ex2_approx(sv[nt][1] - m_ref[0]);
+            const float p2 = ex2_approx(sv[nt][2] - m_ref[1]);
+            const float p3 = ex2_approx(sv[nt][3] - m_ref[1]);
+            l_run[0] += p0 + p1;
+            l_run[1] += p2 + p3;
+            const float r0 = sc[nt][0] * inv_sigma, r1 = sc[nt][1] * inv_sigma;
+            pa[nt >> 1][(nt & 1) * 2 + 0] = pack_f16x2(p0 * r0, p1 * r1);
+            pa[nt >> 1][(nt & 1) * 2 + 1] = pack_f16x2(p2 * r0, p3 * r1);
         }
 
-        // ---- epilogue ----
-        if (ok && nblk > 0)
-            ok = wait_or_abort(&empty[(nblk - 1) & 1], static_cast<uint32_t>(((nblk - 1) >> 1) & 1), abort_flag);
-        tc::fence_after_sync();
-        if (!bar_sync_or(1, kComputeThreads, !ok)) {
-            float* rw = red + qd * 32;
+        // PV: V rows j as K, dims of tile `warp` as N.
 #pragma unroll
-            for (int h = 0; h < kHG; ++h) {
-                const float lh = warp_sum(l_part[h]);
-                if (lane == 0) rw[h] = lh;
+        for (int kb = 0; kb < 2; ++kb) {
+            const uint8_t* vb = st + 128 * warp + 4 * g;
+            const int j0 = 16 * kb + 2 * c;
+#pragma unroll
+            for (int qd = 0; qd < 4; ++qd) {
+                const uint32_t W0 = *reinterpret_cast<const uint32_t*>(vb + (j0 + 0) * kRowBytes + 32 * qd);
+                const uint32_t W1 = *reinterpret_cast<const uint32_t*>(vb + (j0 + 1) * kRowBytes + 32 * qd);
+                const uint32_t W2 = *reinterpret_cast<const uint32_t*>(vb + (j0 + 8) * kRowBytes + 32 * qd);
+                const uint32_t W3 = *reinterpret_cast<const uint32_t*>(vb + (j0 + 9) * kRowBytes + 32 * qd);
+                uint32_t b0a, b0b, b0c, b0d, b1a, b1b, b1c, b1d;
+                e4m3x4_to_f16x2x2(prmt(W0, W1, 0x5140), b0a, b0b);   // d offsets 0, 1
+                e4m3x4_to_f16x2x2(prmt(W0, W1, 0x7362), b0c, b0d);   // d offsets 2, 3
+                e4m3x4_to_f16x2x2(prmt(W2, W3, 0x5140), b1a, b1b);
+                e4m3x4_to_f16x2x2(prmt(W2, W3, 0x7362), b1c, b1d);
+                mma_f16(o[4 * qd + 0], pa[kb], b0a, b1a);
+                mma_f16(o[4 * qd + 1], pa[kb], b0b, b1b);
+                mma_f16(o[4 * qd + 2], pa[kb], b0c, b1c);
+                mma_f16(o[4 * qd + 3], pa[kb], b0d, b1d);
             }
-            bar_sync_or(1, kComputeThreads, false);
-            float mult[kHG];
-#pragma unroll
-            for (int h = 0; h < kHG; ++h) {
-                const float lh = (red[h] + red[32 + h]) + (red[64 + h] + red[96 + h]);
-                mult[h] = lh > 0.0f ? 1.0f / (kPScale * lh) : 0.0f;
-                l_part[h] = lh;
-            }
-#pragma unroll
-            for (int tt = 0; tt < 4; ++tt) {
-                uint32_t ov[16];
-                if (nblk > 0) {
-                    tc::tmem_ld16(tmem + lane_base + kColO + 16 * tt, ov);
-                    tc::wait_ld();
-                } else {
-#pragma unroll
-                    for (int h = 0; h < kHG; ++h) ov[h] = 0u;
-                }
-                const int d = 128 * tt + j;
-#pragma unroll
-                for (int h = 0; h < kHG; ++h) {
-                    if (hg * kHG + h >= H) continue;
-                    const float v = __uint_as_float(ov[h]) * sigma[tt] * mult[h];
-                    if (args.nsplit == 1) {
-                        args.out[(qrow0 + h) * kLatent + d] = __float2bfloat16_rn(v);
-                    } else {
-                        const int64_t prow = (static_cast<int64_t>(t) * args.nsplit + split) * H + hg * kHG + h;
-                        args.ws_o[prow * kLatent + d] = v;
-                    }
-                }
-            }
-            if (ct < kHG && hg * kHG + ct < H) {
-                const float lh = l_part[ct];
-                const float lse2 = lh > 0.0f ? (m_ref[ct] + log2f(lh)) * kLn2 : -INFINITY;
-                if (args.nsplit == 1) {
-                    args.lse[qrow0 + ct] = lse2;
-                } else {
-                    args.ws_lse[(static_cast<int64_t>(t) * args.nsplit + split) * H + hg * kHG + ct] = lse2;
-                }
-            }
-        } else if (ct == 0) {
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+    }
+
+    __syncthreads();     // all 5 warps: producer done issuing, consumers done reading
+    if (failed || *issued_s < nblk) {
+        // A wait ran out: record it, let the copies already issued land (bounded)
+        // and leave without touching the outputs.
+        if (threadIdx.x == 0) {
             atomicOr(args.err, MLA_ERR_PIPELINE_TIMEOUT);
+            const int issued = *issued_s;
+            for (int bb = max(0, issued - kStages); bb < issued; ++bb)
+                (void)mbar_wait_bounded(&full[bb % kStages], static_cast<uint32_t>((bb / kStages) & 1));
         }
+        return;
     }
 
-    // ---- teardown: copies landed, MMAs done, tensor memory released ----
-    __syncthreads();
-    if (threadIdx.x == 0 && *abort_flag) {
-        atomicOr(args.err, MLA_ERR_PIPELINE_TIMEOUT);
-        const int issued = *issued_s;
-        for (int bb = max(0, issued - 2); bb < issued; ++bb)
-            (void)mbar_wait_bounded(&full[bb & 1], static_cast<uint32_t>((bb >> 1) & 1));
+    // ---- epilogue ----
+    float lt[2];
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+        float l = l_run[r];
+        l += __shfl_xor_sync(0xffffffffu, l, 1);
+        l += __shfl_xor_sync(0xffffffffu, l, 2);
+        lt[r] = l;
     }
-    __syncthreads();
-    if (warp == 1) {
-        tc::fence_after_sync();
-        tc::tmem_dealloc(tmem, kTmemCols);
+    const float mult[2] = {lt[0] > 0.0f ? sigma / lt[0] : 0.0f, lt[1] > 0.0f ? sigma / lt[1] : 0.0f};
+    const float lse_r[2] = {lt[0] > 0.0f ? (m_ref[0] + log2f(lt[0])) * kLn2 : -INFINITY,
+                            lt[1] > 0.0f ? (m_ref[1] + log2f(lt[1])) * kLn2 : -INFINITY};
+    const int hs[2] = {h_lo, h_hi};
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+        const int h = hs[r];
+        if (h >= H) continue;
+        const int i0 = 2 * r, i1 = 2 * r + 1;
+        const float mm = mult[r];
+        if (args.nsplit == 1) {
+            __nv_bfloat16* orow = args.out + (static_cast<int64_t>(t) * H + h) * kLatent + 128 * warp + 8 * c;
+#pragma unroll
+            for (int qd = 0; qd < 4; ++qd) {
+                uint4 v;
+                v.x = pack_bf16x2(o[4 * qd + 0][i0] * mm, o[4 * qd + 1][i0] * mm);
+                v.y = pack_bf16x2(o[4 * qd + 2][i0] * mm, o[4 * qd + 3][i0] * mm);
+                v.z = pack_bf16x2(o[4 * qd + 0][i1] * mm, o[4 * qd + 1][i1] * mm);
+                v.w = pack_bf16x2(o[4 * qd + 2][i1] * mm, o[4 * qd + 3][i1] * mm);
+                st_v4(orow + 32 * qd, v);
+            }
+            if (warp == 0 && c == 0) args.lse[static_cast<int64_t>(t) * H + h] = lse_r[r];
+        } else {
+            const int64_t prow = (static_cast<int64_t>(t) * args.nsplit + split) * H + h;
+            float* orow = args.ws_o + prow * kLatent + 128 * warp + 8 * c;
+#pragma unroll
+            for (int qd = 0; qd < 4; ++qd) {
+                reinterpret_cast<float4*>(orow + 32 * qd)[0] =
+                    make_float4(o[4 * qd + 0][i0] * mm, o[4 * qd + 1][i0] * mm, o[4 * qd + 2][i0] * mm, o[4 * qd + 3][i0] * mm);
+                reinterpret_cast<float4*>(orow + 32 * qd)[1] =
+                    make_float4(o[4 * qd + 0][i1] * mm, o[4 * qd + 1][i1] * mm, o[4 * qd + 2][i1] * mm, o[4 * qd + 3][i1] * mm);
+            }
+            if (warp == 0 && c == 0) args.ws_lse[prow] = lse_r[r];
+        }
     }
 }
 
@@ -620,14 +489,14 @@ mla_split_combine_kernel(const float* __restrict__ ws_o, const float* __restrict
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Splits of each token's top-k list: about two CTAs per SM overall (one CTA
-// per SM is resident), at least 128 positions per split, at most kListMax.
+// Number of splits of each token's top-k list: enough CTAs for about four per
+// SM, at least 64 positions per split, and at most kListMax positions per split.
 int choose_nsplit(int T, int H, int W, int sms) {
     if (T <= 0 || W <= 0) return 1;
-    const int64_t base = static_cast<int64_t>(T) * ((H + kHG - 1) / kHG);
-    const int64_t target = 2ll * sms;
+    const int64_t base = static_cast<int64_t>(T) * ((H + kHeads - 1) / kHeads);
+    const int64_t target = 4ll * sms;
     int64_t ns = (target + base - 1) / base;
-    const int64_t max_ns = (W >= 128) ? W / 128 : 1;
+    const int64_t max_ns = (W >= 64) ? W / 64 : 1;
     if (ns > max_ns) ns = max_ns;
     const int64_t min_ns = (W + kListMax - 1) / kListMax;
     if (ns < min_ns) ns = min_ns;
@@ -640,37 +509,6 @@ size_t workspace_for(int T, int H, int nsplit) {
     const size_t rows = static_cast<size_t>(T) * nsplit * H;
     const size_t o_bytes = rows * kLatent * sizeof(float);
     return o_bytes + ((rows * sizeof(float) + 255) & ~static_cast<size_t>(255));
-}
-
-// ---- TMA tensor maps over the cache (driver entry point, looked up once) ----
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-    static std::once_flag once;
-    static EncodeTiledFn fn = nullptr;
-    std::call_once(once, []() {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(p);
-    });
-    return fn;
-}
-
-// Cache viewed as a 2-D byte tensor [rows, 656]; boxes one row high (gather4).
-bool make_row_map(CUtensorMap* m, void* data, int64_t rows, uint32_t box_bytes, CUtensorMapSwizzle sw) {
-    EncodeTiledFn fn = encode_fn();
-    if (fn == nullptr) return false;
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kRowBytes), static_cast<cuuint64_t>(rows)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kRowBytes)};
-    const cuuint32_t box[2] = {box_bytes, 1};
-    const cuuint32_t estr[2] = {1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, data, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-              sw, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace
@@ -689,7 +527,6 @@ extern "C" int mla_sparse_decode(const void* q_bf16, int T, int H, int d_qk, mla
         return MLA_EINVAL;
     if (d_qk != kLatent && d_qk != kLatent + kRope) return MLA_EUNSUPPORTED;
     if (H < 1 || H > 128) return MLA_EUNSUPPORTED;
-    if (kv.num_slots >= INT32_MAX) return MLA_EUNSUPPORTED;     // row coordinates are 32-bit
     if (T == 0) return MLA_OK;
     if (q_bf16 == nullptr || out_bf16 == nullptr || lse == nullptr || (W > 0 && topk_idx == nullptr) ||
         (W > 0 && kv.data == nullptr))
@@ -709,27 +546,16 @@ extern "C" int mla_sparse_decode(const void* q_bf16, int T, int H, int d_qk, mla
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MLA_ECUDA;
     if (!attr_set[dev]) {
-        if (cudaFuncSetAttribute(mla_sparse_decode_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kSmemAlloc) != cudaSuccess ||
-            cudaFuncSetAttribute(mla_sparse_decode_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kSmemAlloc) != cudaSuccess)
+        if (cudaFuncSetAttribute(mla_sparse_decode_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kSmemTotal) != cudaSuccess ||
+            cudaFuncSetAttribute(mla_sparse_decode_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kSmemTotal) != cudaSuccess)
             return MLA_ECUDA;
         attr_set[dev] = true;
     }
-    // Tensor maps: rows are 1 .. num_slots-1 at most; a coordinate >= the row
-    // count reads as zeros (used for the ragged end of a block).
-    alignas(64) CUtensorMap tm_row;
-    alignas(64) CUtensorMap tm_scale;
-    std::memset(&tm_row, 0, sizeof tm_row);
-    std::memset(&tm_scale, 0, sizeof tm_scale);
-    const int64_t rows = kv.num_slots > 0 ? kv.num_slots : 1;
-    if (W > 0) {
-        if (!make_row_map(&tm_row, kv.data, rows, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
-            !make_row_map(&tm_scale, kv.data, rows, 16, CU_TENSOR_MAP_SWIZZLE_NONE))
-            return MLA_ECUDA;
-    }
     DecodeArgs a;
     a.q = static_cast<const __nv_bfloat16*>(q_bf16);
+    a.cache = static_cast<const uint8_t*>(kv.data);
     a.topk = topk_idx;
     a.out = static_cast<__nv_bfloat16*>(out_bf16);
     a.lse = lse;
@@ -739,16 +565,15 @@ extern "C" int mla_sparse_decode(const void* q_bf16, int T, int H, int d_qk, mla
                           : nullptr;
     a.err = err;
     a.num_slots = kv.num_slots;
-    a.oob_row = static_cast<int>(rows);
     a.T = T; a.H = H; a.d_qk = d_qk; a.W = W; a.nsplit = nsplit;
     a.split_len = (W + nsplit - 1) / nsplit;
     a.sm_scale_log2 = sm_scale * kLog2e;
-    const dim3 grid(static_cast<unsigned>(T), static_cast<unsigned>(nsplit), static_cast<unsigned>((H + kHG - 1) / kHG));
+    const dim3 grid(static_cast<unsigned>(T), static_cast<unsigned>(nsplit), static_cast<unsigned>((H + kHeads - 1) / kHeads));
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (d_qk == kLatent + kRope)
-        mla_sparse_decode_tc_kernel<true><<<grid, kThreads, kSmemAlloc, st>>>(tm_row, tm_scale, a);
+        mla_sparse_decode_kernel<true><<<grid, kThreads, kSmemTotal, st>>>(a);
     else
-        mla_sparse_decode_tc_kernel<false><<<grid, kThreads, kSmemAlloc, st>>>(tm_row, tm_scale, a);
+        mla_sparse_decode_kernel<false><<<grid, kThreads, kSmemTotal, st>>>(a);
     if (cudaGetLastError() != cudaSuccess) return MLA_ECUDA;
     if (nsplit > 1) {
         mla_split_combine_kernel<<<static_cast<unsigned>(static_cast<int64_t>(T) * H), 128, 0, st>>>(
