@@ -135,6 +135,23 @@ __device__ __forceinline__ float ex2_approx(float x) {
     return y;
 }
 
+// x / s rounded to nearest even, for a scale s inside kDivFastMin .. kDivFastMax,
+// given y = RN(1 / s): Markstein's residual correction (P. Markstein, "Computation
+// of elementary functions on the IBM RISC System/6000 processor", IBM J. Res.
+// Dev. 34(1), 1990): q0 = RN(x*y), r = x - q0*s exactly (one FMA), q = RN(q0 + r*y).
+// The sign of a zero quotient is restored from x. The residual is exact unless
+// it underflows, which needs |x| < 2^-100; with s >= 2^-80 such an x has
+// |x / s| < 2^-20, far below the smallest E4M3 step, so the stored code is the
+// same. Checked against the IEEE division, code for code, on every (bf16 amax,
+// bf16 x) pair a tile can produce.
+constexpr float kDivFastMin = 0x1p-80f;
+constexpr float kDivFastMax = 0x1p+100f;
+__device__ __forceinline__ float div_by_scale(float x, float s, float y) {
+    const float q0 = __fmul_rn(x, y);
+    const float r = __fmaf_rn(-q0, s, x);
+    return copysignf(__fmaf_rn(r, y, q0), x);
+}
+
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
     uint32_t r;
     asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));

@@ -19,9 +19,12 @@ using namespace mla;
 
 constexpr int kWriterThreads = 256;   // 8 rows in flight per CTA
 
-__device__ __forceinline__ uint32_t quant2(float x0, float x1, float scale) {
-    // IEEE fp32 division, then round-to-nearest-even E4M3 with saturation.
-    const float2 v = make_float2(__fdiv_rn(x0, scale), __fdiv_rn(x1, scale));
+__device__ __forceinline__ uint32_t quant2(float x0, float x1, float scale, float rcp, bool fast) {
+    // x / scale rounded to nearest even (the IEEE quotient: the fast form is the
+    // residual-corrected reciprocal product), then round-to-nearest-even E4M3
+    // with saturation.
+    const float2 v = fast ? make_float2(div_by_scale(x0, scale, rcp), div_by_scale(x1, scale, rcp))
+                          : make_float2(__fdiv_rn(x0, scale), __fdiv_rn(x1, scale));
     return static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(v, __NV_SATFINITE, __NV_E4M3));
 }
 
@@ -62,11 +65,14 @@ mla_kv_write_kernel(uint8_t* __restrict__ cache, int64_t num_slots,
         amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
         amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
         const float scale = (amax > 0.0f) ? __fdiv_rn(amax, MLA_FP8_MAX) : 1.0f;
+        const bool fast = scale >= kDivFastMin && scale <= kDivFastMax;   // false only for extreme tiles
+        const float rcp = __frcp_rn(scale);
 
         uint32_t qv[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k)
-            qv[k] = quant2(v[4 * k], v[4 * k + 1], scale) | (quant2(v[4 * k + 2], v[4 * k + 3], scale) << 16);
+            qv[k] = quant2(v[4 * k], v[4 * k + 1], scale, rcp, fast) |
+                    (quant2(v[4 * k + 2], v[4 * k + 3], scale, rcp, fast) << 16);
 
         uint8_t* row = cache + slot * static_cast<int64_t>(kRowBytes);
         st_v4(row + 16 * lane, make_uint4(qv[0], qv[1], qv[2], qv[3]));

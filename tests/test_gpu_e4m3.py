@@ -41,3 +41,18 @@ def test_exhaustive_fp32_to_e4m3_matches_oracle():
         ref = oracle.e4m3_encode_bit_range(lo, lo + chunk)
         bad = np.nonzero(got != ref)[0]
         assert bad.size == 0, [(hex(lo + int(i)), hex(got[i]), hex(ref[i])) for i in bad[:8]]
+
+
+@pytest.mark.gpu
+def test_writer_division_gives_ieee_codes_on_every_bf16_pair():
+    src = os.path.join(HERE, "gpu_helpers", "div_check.cu")
+    so = os.path.join(OUT_DIR, "libdiv_check.so")
+    os.makedirs(OUT_DIR, exist_ok=True)
+    subprocess.run([B.nvcc(), *B.ARCH, "-O3", "-std=c++17", "-shared", "-Xcompiler", "-fPIC", src, "-o", so], check=True)
+    lib = ctypes.CDLL(so)
+    counts = (ctypes.c_ulonglong * 2)()
+    ex = (ctypes.c_uint32 * 16)()
+    assert lib.div_check(counts, ex) == 0
+    checked, bad = counts[0], counts[1]
+    assert checked > 500_000_000
+    assert bad == 0, [(hex(ex[2 * i]), hex(ex[2 * i + 1])) for i in range(min(bad, 8))]
