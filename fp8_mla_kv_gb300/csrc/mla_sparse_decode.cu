@@ -8,23 +8,28 @@
 // shared memory, so -1, slot 0 and out-of-range indices are never dereferenced.
 //
 // Work decomposition: one CTA per (token, split of the top-k list, group of 16
-// heads); 4 warps; warp w owns latent tile w (dims 128w .. 128w+127) and RoPE
-// dims 16w .. 16w+15. Present rows move global -> shared with one
-// cp.async.bulk per row (656 B, or 528 B for NoPE: the tail is not read) into
-// a 4-stage ring of 32-row blocks, each stage completing on an mbarrier.
+// heads); 4 consumer warps and 1 producer warp. Every thread loads a contiguous
+// run of the split's positions at once (the q loads are issued before them) and
+// one block-wide scan places the present ones in a shared-memory list. The
+// producer copies each listed row global -> shared with one cp.async.bulk (656 B,
+// or 528 B for NoPE: the tail is not read) into a 4-stage ring of 32-row blocks,
+// each stage completing on an mbarrier.
 //
 // Arithmetic per 32-row block, on tensor cores (m16n8k16, heads as M):
-//   QK  : the E4M3 latent goes to f16 exactly (cvt.f16x2.e4m3x2); q goes to f16
-//         exactly after an exponent-only per-head rescale that keeps it in f16
-//         range; the per-row, per-tile fp32 scale multiplies each warp's tile
-//         partial afterwards, so the product q.K is exact before fp32
-//         accumulation. RoPE dims run as a bf16 MMA on the stored bf16 values.
-//   softmax: the four tile partials are summed through shared memory; online
-//         max / sum in fp32 with exp2 (log2 e folded into sm_scale).
-//   PV  : p * scale_row / sigma (sigma = running max of the tile's scales, so the
-//         f16 operand stays in [0, 1]) times the exact f16 E4M3 codes; O stays
-//         in registers (16 heads x 128 dims per warp) and is rescaled with the
-//         softmax correction.
+//   QK  : warp w takes latent tile w (dims 128w .. 128w+127) and RoPE dims
+//         16w .. 16w+15 for all 32 rows. The E4M3 latent goes to f16 exactly
+//         (cvt.f16x2.e4m3x2); q goes to f16 exactly after an exponent-only
+//         per-head rescale that keeps it in f16 range; the per-row, per-tile
+//         fp32 scale multiplies each tile partial afterwards, so q.K is exact
+//         before fp32 accumulation. RoPE dims run as a bf16 MMA.
+//   softmax: the four tile partials meet in shared memory and warp w finishes
+//         the scores of rows 8w .. 8w+7 only; online max / sum in fp32 with exp2
+//         (log2 e folded into sm_scale). The exp2 offset of a head is shared by
+//         all warps and moves only when a block maximum runs more than
+//         kRescaleSlack above it, so P <= 2^8 fits the f16 operand.
+//   PV  : warp w owns output dims 128w .. 128w+127; P (f16, from shared memory)
+//         times scale_row / sigma (sigma = running max of tile w's scales) times
+//         the exact f16 E4M3 codes, with 16-byte V loads; O stays in registers.
 // Splits write a normalised partial (o, lse) to the caller's workspace and a
 // second kernel merges them in split order (deterministic: no float atomics).
 #include <cfloat>
@@ -44,13 +49,15 @@ constexpr int kConsumerThreads = kWarps * 32;
 constexpr int kNB = 32;                      // rows per block
 constexpr int kStages = 4;
 constexpr int kListMax = 2304;               // positions one CTA compacts
+constexpr int kPerThread = (kListMax + kThreads - 1) / kThreads;   // positions per thread in the compaction
 constexpr int kStageBytes = kNB * kRowBytes; // 20,992
 constexpr int kSmemStages = kStages * kStageBytes;
 constexpr int kSmemList = kListMax * 4;
-constexpr int kSmemRed = 2 * kWarps * 4 * 32 * 16;   // two buffers of float4 [warp][n-tile][lane]
-constexpr int kSmemQmax = kWarps * kHeads * 4;
-constexpr int kSmemMisc = 16 + 2 * kStages * 8 + 16; // warp counts, full + empty barriers, issued count
-constexpr int kSmemTotal = kSmemStages + kSmemList + kSmemRed + kSmemQmax + kSmemMisc;
+constexpr int kSmemRed = kWarps * 4 * 32 * 16;       // QK tile partials: float4 [warp][n-tile][lane]
+constexpr int kSmemP = 4 * 32 * 8;                   // P (f16): uint2 [n-tile][lane], A-fragment order
+constexpr int kSmemQmax = 3 * kWarps * kHeads * 4;   // |q| maxima, block score maxima, l partials
+constexpr int kSmemMisc = 32 + 2 * kStages * 8 + 16; // warp counts, full + empty barriers, issued count
+constexpr int kSmemTotal = kSmemStages + kSmemList + kSmemRed + kSmemP + kSmemQmax + kSmemMisc;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 // The running max used as the exp2 offset is only moved when a score exceeds it
@@ -83,9 +90,12 @@ mla_sparse_decode_kernel(const DecodeArgs args) {
     uint8_t* stages = smem;
     int* list = reinterpret_cast<int*>(smem + kSmemStages);
     float4* red = reinterpret_cast<float4*>(smem + kSmemStages + kSmemList);
-    float* qmax_s = reinterpret_cast<float*>(smem + kSmemStages + kSmemList + kSmemRed);
-    int* wcount = reinterpret_cast<int*>(smem + kSmemStages + kSmemList + kSmemRed + kSmemQmax);
-    uint64_t* full = reinterpret_cast<uint64_t*>(wcount + 4);
+    uint32_t* pbuf = reinterpret_cast<uint32_t*>(smem + kSmemStages + kSmemList + kSmemRed);
+    float* qmax_s = reinterpret_cast<float*>(smem + kSmemStages + kSmemList + kSmemRed + kSmemP);
+    float* rmax_s = qmax_s + kWarps * kHeads;
+    float* lsum_s = rmax_s + kWarps * kHeads;
+    int* wcount = reinterpret_cast<int*>(smem + kSmemStages + kSmemList + kSmemRed + kSmemP + kSmemQmax);
+    uint64_t* full = reinterpret_cast<uint64_t*>(wcount + 8);
     uint64_t* empty = full + kStages;
     int* issued_s = reinterpret_cast<int*>(empty + kStages);
 
@@ -106,30 +116,74 @@ mla_sparse_decode_kernel(const DecodeArgs args) {
         fence_mbar_init();
     }
 
+    // ---- 0. q of this token and head group (consumer warps), loads issued first ----
+    const int g = lane >> 2;
+    const int c = lane & 3;
+    const int h_lo = hg * kHeads + g;
+    const int h_hi = h_lo + 8;
+    uint32_t qraw[2][16];
+    uint32_t qr[2][2];
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+        const int h = r ? h_hi : h_lo;
+        qr[r][0] = qr[r][1] = 0u;
+#pragma unroll
+        for (int k = 0; k < 16; ++k) qraw[r][k] = 0u;
+        if (warp < kWarps && h < H) {
+            const __nv_bfloat16* qh = args.q + (static_cast<int64_t>(t) * H + h) * args.d_qk;
+            const uint8_t* p = reinterpret_cast<const uint8_t*>(qh + 128 * warp + 32 * c);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const uint4 v = ld_nc_v4(p + 16 * k);
+                qraw[r][4 * k + 0] = v.x; qraw[r][4 * k + 1] = v.y;
+                qraw[r][4 * k + 2] = v.z; qraw[r][4 * k + 3] = v.w;
+            }
+            if (kRopeOn) {
+                const uint2 v = *reinterpret_cast<const uint2*>(qh + kLatent + 16 * warp + 4 * c);
+                qr[r][0] = v.x; qr[r][1] = v.y;
+            }
+        }
+    }
+
     // ---- 1. compact the present entries of this split's positions (all warps) ----
+    // Thread i takes a contiguous run of `per` positions, loaded all at once; one
+    // block-wide scan of the per-thread counts places them in position order.
     const int p0 = split * args.split_len;
     const int p1 = min(args.W, p0 + args.split_len);
-    const int32_t* trow = args.topk + static_cast<int64_t>(t) * args.W;
-    int n_valid = 0;
-    for (int base = p0; base < p1; base += kConsumerThreads) {
-        const int pos = base + threadIdx.x;
-        const int idx = (warp < kWarps && pos < p1) ? __ldg(trow + pos) : -1;
+    const int per = (max(0, p1 - p0) + kThreads - 1) / kThreads;     // <= kPerThread
+    const int32_t* trow = args.topk + static_cast<int64_t>(t) * args.W + p0 + threadIdx.x * per;
+    const int mine = max(0, min(per, p1 - (p0 + static_cast<int>(threadIdx.x) * per)));
+    int idxv[kPerThread];
+#pragma unroll
+    for (int k = 0; k < kPerThread; ++k) idxv[k] = (k < mine) ? __ldg(trow + k) : -1;
+    int cnt = 0;
+#pragma unroll
+    for (int k = 0; k < kPerThread; ++k) {
+        const int idx = idxv[k];
         const bool valid = idx > 0 && static_cast<int64_t>(idx) < args.num_slots;
         if (idx > 0 && !valid) atomicOr(args.err, MLA_ERR_DECODE_INDEX_RANGE);
-        const unsigned m = __ballot_sync(0xffffffffu, valid);
-        if (lane == 0 && warp < kWarps) wcount[warp] = __popc(m);
-        __syncthreads();
-        int off = n_valid, total = 0;
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) {
-            const int cw = wcount[w];
-            off += (w < warp) ? cw : 0;
-            total += cw;
-        }
-        if (valid) list[off + __popc(m & ((1u << lane) - 1u))] = idx;
-        n_valid += total;
-        __syncthreads();
+        idxv[k] = valid ? idx : 0;
+        cnt += valid ? 1 : 0;
     }
+    int incl = cnt;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, d);
+        if (lane >= d) incl += v;
+    }
+    if (lane == 31) wcount[warp] = incl;
+    __syncthreads();
+    int off = incl - cnt, n_valid = 0;
+#pragma unroll
+    for (int w = 0; w < kThreads / 32; ++w) {
+        const int cw = wcount[w];
+        off += (w < warp) ? cw : 0;
+        n_valid += cw;
+    }
+#pragma unroll
+    for (int k = 0; k < kPerThread; ++k)
+        if (idxv[k] != 0) list[off++] = idxv[k];
+    __syncthreads();
     const int nblk = (n_valid + kNB - 1) / kNB;
 
     if (warp == kProducer) {
@@ -165,35 +219,10 @@ mla_sparse_decode_kernel(const DecodeArgs args) {
     }
 
     // ---- consumers: q fragments ----
-    const int g = lane >> 2;
-    const int c = lane & 3;
-    const int h_lo = hg * kHeads + g;
-    const int h_hi = h_lo + 8;
-    uint32_t qraw[2][16];
-    uint32_t qr[2][2];
     float qm[2];
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
-        const int h = r ? h_hi : h_lo;
         qm[r] = 0.0f;
-        qr[r][0] = qr[r][1] = 0u;
-        if (h < H) {
-            const __nv_bfloat16* qh = args.q + (static_cast<int64_t>(t) * H + h) * args.d_qk;
-            const uint8_t* p = reinterpret_cast<const uint8_t*>(qh + 128 * warp + 32 * c);
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const uint4 v = ld_nc_v4(p + 16 * k);
-                qraw[r][4 * k + 0] = v.x; qraw[r][4 * k + 1] = v.y;
-                qraw[r][4 * k + 2] = v.z; qraw[r][4 * k + 3] = v.w;
-            }
-            if (kRopeOn) {
-                const uint2 v = *reinterpret_cast<const uint2*>(qh + kLatent + 16 * warp + 4 * c);
-                qr[r][0] = v.x; qr[r][1] = v.y;
-            }
-        } else {
-#pragma unroll
-            for (int k = 0; k < 16; ++k) qraw[r][k] = 0u;
-        }
 #pragma unroll
         for (int k = 0; k < 16; ++k) qm[r] = fmaxf(qm[r], fmaxf(fabsf(bf16lo(qraw[r][k])), fabsf(bf16hi(qraw[r][k]))));
 #pragma unroll
@@ -239,12 +268,18 @@ mla_sparse_decode_kernel(const DecodeArgs args) {
     qra[3] = pack_bf16x2(bf16lo(qr[1][1]) * qdown[1], bf16hi(qr[1][1]) * qdown[1]);
 
     // ---- consumers: main loop ----
+    // Per 32-row block: (1) QK partial of tile `warp` for all 32 rows, (2) the
+    // four tile partials meet in shared memory and warp w finishes the scores of
+    // rows 8w .. 8w+7 (its n-tile) and writes their P, (3) every warp multiplies
+    // all 32 rows of P into V of its own tile. Two barriers per block; the exp2
+    // offset of each head is common to all warps and moves only when a block
+    // maximum runs more than kRescaleSlack above it (a third barrier then).
     float o[16][4];
 #pragma unroll
     for (int i = 0; i < 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.0f;
-    float m_ref[2] = {-INFINITY, -INFINITY};   // exp2 offset per row (log2 units)
-    float l_run[2] = {0.0f, 0.0f};
-    float sigma = FLT_MIN;                     // running max of this tile's row scales
+    float m_ref[2] = {-INFINITY, -INFINITY};   // exp2 offset per head row (log2 units)
+    float l_run[2] = {0.0f, 0.0f};             // sum of p over this warp's rows
+    float sigma = FLT_MIN;                     // running max of tile `warp`'s row scales
     float inv_sigma = 1.0f / FLT_MIN;
     bool failed = false;
 
@@ -254,7 +289,7 @@ mla_sparse_decode_kernel(const DecodeArgs args) {
         const uint8_t* st = stages + s * kStageBytes;
         const int n_b = min(kNB, n_valid - b * kNB);
 
-        // QK^T: latent on f16 MMA (4 independent accumulators per k-step).
+        // (1) QK^T of tile `warp`: latent on f16 MMA, RoPE slice on bf16 MMA.
         float acc[4][4], accr[4][4];
 #pragma unroll
         for (int nt = 0; nt < 4; ++nt)
@@ -284,110 +319,131 @@ mla_sparse_decode_kernel(const DecodeArgs args) {
                 mma_bf16(accr[nt], qra, rb.x, rb.y);
             }
         }
-        // Row scale of tile `warp` for the 8 columns this thread holds
-        // (rows past n_b were zero-filled: scale 0).
+        // Scale of tile `warp` for rows nt*8 + 2c + e (rows past n_b were
+        // zero-filled: scale 0). The same registers serve the PV step.
         float sc[4][2];
 #pragma unroll
         for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
             for (int e = 0; e < 2; ++e)
                 sc[nt][e] = *reinterpret_cast<const float*>(st + (nt * 8 + 2 * c + e) * kRowBytes + kScaleOff + 4 * warp);
-        float4* rbuf = red + (b & 1) * (kWarps * 4 * 32);
 #pragma unroll
         for (int nt = 0; nt < 4; ++nt)
-            rbuf[(warp * 4 + nt) * 32 + lane] =
+            red[(warp * 4 + nt) * 32 + lane] =
                 make_float4(fmaf(acc[nt][0], sc[nt][0], accr[nt][0]), fmaf(acc[nt][1], sc[nt][1], accr[nt][1]),
                             fmaf(acc[nt][2], sc[nt][0], accr[nt][2]), fmaf(acc[nt][3], sc[nt][1], accr[nt][3]));
-        // One barrier per block for the four consumer warps; it also carries a
-        // timeout of any of them to all of them.
+        // Barrier 1 also carries a timeout of any warp to all of them.
         if (bar_sync_or(1, kConsumerThreads, !ok)) { failed = true; break; }
-        float sv[4][4];
+
+        // (2) scores of n-tile `warp`: rows 8*warp + 2c + {0,1}, heads g and g+8.
+        float4 a = red[warp * 32 + lane];
 #pragma unroll
-        for (int nt = 0; nt < 4; ++nt) {
-            float4 a = rbuf[nt * 32 + lane];
-#pragma unroll
-            for (int w = 1; w < kWarps; ++w) {
-                const float4 bq = rbuf[(w * 4 + nt) * 32 + lane];
-                a.x += bq.x; a.y += bq.y; a.z += bq.z; a.w += bq.w;
-            }
-            sv[nt][0] = a.x * rowf[0]; sv[nt][1] = a.y * rowf[0];
-            sv[nt][2] = a.z * rowf[1]; sv[nt][3] = a.w * rowf[1];
+        for (int w = 1; w < kWarps; ++w) {
+            const float4 bq = red[(w * 4 + warp) * 32 + lane];
+            a.x += bq.x; a.y += bq.y; a.z += bq.z; a.w += bq.w;
         }
+        float sv[4] = {a.x * rowf[0], a.y * rowf[0], a.z * rowf[1], a.w * rowf[1]};
         if (n_b < kNB) {
 #pragma unroll
-            for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    if (nt * 8 + 2 * c + (i & 1) >= n_b) sv[nt][i] = -INFINITY;
+            for (int i = 0; i < 4; ++i)
+                if (8 * warp + 2 * c + (i & 1) >= n_b) sv[i] = -INFINITY;
         }
-        float rmax[2] = {-INFINITY, -INFINITY};
-        float smax = 0.0f;
-#pragma unroll
-        for (int nt = 0; nt < 4; ++nt) {
-            rmax[0] = fmaxf(rmax[0], fmaxf(sv[nt][0], sv[nt][1]));
-            rmax[1] = fmaxf(rmax[1], fmaxf(sv[nt][2], sv[nt][3]));
-            smax = fmaxf(smax, fmaxf(sc[nt][0], sc[nt][1]));
+        const float bm0 = quad_max(fmaxf(sv[0], sv[1]));
+        const float bm1 = quad_max(fmaxf(sv[2], sv[3]));
+        if (c == 0) {
+            rmax_s[warp * kHeads + g] = bm0;
+            rmax_s[warp * kHeads + g + 8] = bm1;
         }
-        rmax[0] = quad_max(rmax[0]);
-        rmax[1] = quad_max(rmax[1]);
-        smax = quad_max(smax);
-        const bool move0 = rmax[0] > m_ref[0] + kRescaleSlack;
-        const bool move1 = rmax[1] > m_ref[1] + kRescaleSlack;
-        if (__any_sync(0xffffffffu, move0 || move1 || smax > sigma)) {
-            // Rare after the first blocks: move the exp2 offsets and/or sigma and
-            // rescale O and l accordingly.
-            const float mn0 = move0 ? rmax[0] : m_ref[0];
-            const float mn1 = move1 ? rmax[1] : m_ref[1];
+        const bool need = bm0 > m_ref[0] + kRescaleSlack || bm1 > m_ref[1] + kRescaleSlack;
+        float p[4];
+        p[0] = ex2_approx(sv[0] - m_ref[0]);
+        p[1] = ex2_approx(sv[1] - m_ref[0]);
+        p[2] = ex2_approx(sv[2] - m_ref[1]);
+        p[3] = ex2_approx(sv[3] - m_ref[1]);
+        uint2* pw = reinterpret_cast<uint2*>(pbuf) + warp * 32 + lane;
+        *pw = make_uint2(pack_f16x2(p[0], p[1]), pack_f16x2(p[2], p[3]));
+        if (bar_sync_or(1, kConsumerThreads, need)) {
+            // Rare after the first block: move the offsets of the heads whose
+            // block maximum ran ahead, rescale O and l, and rewrite this warp's P.
+            float M0 = -INFINITY, M1 = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) {
+                M0 = fmaxf(M0, rmax_s[w * kHeads + g]);
+                M1 = fmaxf(M1, rmax_s[w * kHeads + g + 8]);
+            }
+            const float mn0 = (M0 > m_ref[0] + kRescaleSlack) ? M0 : m_ref[0];
+            const float mn1 = (M1 > m_ref[1] + kRescaleSlack) ? M1 : m_ref[1];
             const float a0 = ex2_approx(m_ref[0] - mn0);     // -inf -> 0
             const float a1 = ex2_approx(m_ref[1] - mn1);
-            const float sig_new = fmaxf(sigma, smax);
-            const float rs = sigma / sig_new;
-            const float f0 = a0 * rs, f1 = a1 * rs;
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-                o[i][0] *= f0; o[i][1] *= f0; o[i][2] *= f1; o[i][3] *= f1;
+                o[i][0] *= a0; o[i][1] *= a0; o[i][2] *= a1; o[i][3] *= a1;
             }
             l_run[0] *= a0;
             l_run[1] *= a1;
             m_ref[0] = mn0;
             m_ref[1] = mn1;
-            sigma = sig_new;
-            inv_sigma = 1.0f / sig_new;
+            p[0] = ex2_approx(sv[0] - mn0);
+            p[1] = ex2_approx(sv[1] - mn0);
+            p[2] = ex2_approx(sv[2] - mn1);
+            p[3] = ex2_approx(sv[3] - mn1);
+            *pw = make_uint2(pack_f16x2(p[0], p[1]), pack_f16x2(p[2], p[3]));
+            bar_sync_or(1, kConsumerThreads, false);
         }
-        uint32_t pa[2][4];
-#pragma unroll
-        for (int nt = 0; nt < 4; ++nt) {
-            const float p0 = ex2_approx(sv[nt][0] - m_ref[0]);
-            const float p1 = ex2_approx(sv[nt][1] - m_ref[0]);
-            const float p2 = ex2_approx(sv[nt][2] - m_ref[1]);
-            const float p3 = ex2_approx(sv[nt][3] - m_ref[1]);
-            l_run[0] += p0 + p1;
-            l_run[1] += p2 + p3;
-            const float r0 = sc[nt][0] * inv_sigma, r1 = sc[nt][1] * inv_sigma;
-            pa[nt >> 1][(nt & 1) * 2 + 0] = pack_f16x2(p0 * r0, p1 * r1);
-            pa[nt >> 1][(nt & 1) * 2 + 1] = pack_f16x2(p2 * r0, p3 * r1);
-        }
+        l_run[0] += p[0] + p[1];
+        l_run[1] += p[2] + p[3];
 
-        // PV: V rows j as K, dims of tile `warp` as N.
+        // (3) PV of tile `warp`. sigma keeps p * scale / sigma <= 2^8 in f16.
+        float smax = 0.0f;
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt) smax = fmaxf(smax, fmaxf(sc[nt][0], sc[nt][1]));
+        smax = quad_max(smax);                 // all 32 rows: the same in every lane
+        if (smax > sigma) {
+            const float f = sigma / smax;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                o[i][0] *= f; o[i][1] *= f; o[i][2] *= f; o[i][3] *= f;
+            }
+            sigma = smax;
+            inv_sigma = 1.0f / smax;
+        }
+        const uint2* pr = reinterpret_cast<const uint2*>(pbuf) + lane;
 #pragma unroll
         for (int kb = 0; kb < 2; ++kb) {
-            const uint8_t* vb = st + 128 * warp + 4 * g;
+            // A: P of heads (g, g+8) x rows 16kb + 2c + {0,1} and + 8, times the
+            // row's tile scale / sigma.
+            const uint2 plo = pr[(2 * kb) * 32];
+            const uint2 phi = pr[(2 * kb + 1) * 32];
+            const uint32_t r01 = pack_f16x2(sc[2 * kb][0] * inv_sigma, sc[2 * kb][1] * inv_sigma);
+            const uint32_t r89 = pack_f16x2(sc[2 * kb + 1][0] * inv_sigma, sc[2 * kb + 1][1] * inv_sigma);
+            uint32_t pa[4];
+            pa[0] = hmul2(plo.x, r01);
+            pa[1] = hmul2(plo.y, r01);
+            pa[2] = hmul2(phi.x, r89);
+            pa[3] = hmul2(phi.y, r89);
+            // B: V rows j0, j0+1, j0+8, j0+9; lane g takes dims 128w + 16g .. +15,
+            // so n-tile (q, i) column n is dim 128w + 16n + 4q + i.
             const int j0 = 16 * kb + 2 * c;
+            const uint8_t* vb = st + 128 * warp + 16 * g;
+            const uint4 V0 = *reinterpret_cast<const uint4*>(vb + (j0 + 0) * kRowBytes);
+            const uint4 V1 = *reinterpret_cast<const uint4*>(vb + (j0 + 1) * kRowBytes);
+            const uint4 V2 = *reinterpret_cast<const uint4*>(vb + (j0 + 8) * kRowBytes);
+            const uint4 V3 = *reinterpret_cast<const uint4*>(vb + (j0 + 9) * kRowBytes);
 #pragma unroll
             for (int qd = 0; qd < 4; ++qd) {
-                const uint32_t W0 = *reinterpret_cast<const uint32_t*>(vb + (j0 + 0) * kRowBytes + 32 * qd);
-                const uint32_t W1 = *reinterpret_cast<const uint32_t*>(vb + (j0 + 1) * kRowBytes + 32 * qd);
-                const uint32_t W2 = *reinterpret_cast<const uint32_t*>(vb + (j0 + 8) * kRowBytes + 32 * qd);
-                const uint32_t W3 = *reinterpret_cast<const uint32_t*>(vb + (j0 + 9) * kRowBytes + 32 * qd);
+                const uint32_t W0 = qd == 0 ? V0.x : qd == 1 ? V0.y : qd == 2 ? V0.z : V0.w;
+                const uint32_t W1 = qd == 0 ? V1.x : qd == 1 ? V1.y : qd == 2 ? V1.z : V1.w;
+                const uint32_t W2 = qd == 0 ? V2.x : qd == 1 ? V2.y : qd == 2 ? V2.z : V2.w;
+                const uint32_t W3 = qd == 0 ? V3.x : qd == 1 ? V3.y : qd == 2 ? V3.z : V3.w;
                 uint32_t b0a, b0b, b0c, b0d, b1a, b1b, b1c, b1d;
                 e4m3x4_to_f16x2x2(prmt(W0, W1, 0x5140), b0a, b0b);   // d offsets 0, 1
                 e4m3x4_to_f16x2x2(prmt(W0, W1, 0x7362), b0c, b0d);   // d offsets 2, 3
                 e4m3x4_to_f16x2x2(prmt(W2, W3, 0x5140), b1a, b1b);
                 e4m3x4_to_f16x2x2(prmt(W2, W3, 0x7362), b1c, b1d);
-                mma_f16(o[4 * qd + 0], pa[kb], b0a, b1a);
-                mma_f16(o[4 * qd + 1], pa[kb], b0b, b1b);
-                mma_f16(o[4 * qd + 2], pa[kb], b0c, b1c);
-                mma_f16(o[4 * qd + 3], pa[kb], b0d, b1d);
+                mma_f16(o[4 * qd + 0], pa, b0a, b1a);
+                mma_f16(o[4 * qd + 1], pa, b0b, b1b);
+                mma_f16(o[4 * qd + 2], pa, b0c, b1c);
+                mma_f16(o[4 * qd + 3], pa, b0d, b1d);
             }
         }
         __syncwarp();
@@ -407,46 +463,57 @@ mla_sparse_decode_kernel(const DecodeArgs args) {
         return;
     }
 
-    // ---- epilogue ----
-    float lt[2];
+    // ---- epilogue: l over the four warps' rows, then O * sigma / l ----
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
         float l = l_run[r];
         l += __shfl_xor_sync(0xffffffffu, l, 1);
         l += __shfl_xor_sync(0xffffffffu, l, 2);
-        lt[r] = l;
+        if (c == 0) lsum_s[warp * kHeads + g + 8 * r] = l;
+    }
+    bar_sync_or(1, kConsumerThreads, false);
+    float lt[2] = {0.0f, 0.0f};
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+        lt[0] += lsum_s[w * kHeads + g];
+        lt[1] += lsum_s[w * kHeads + g + 8];
     }
     const float mult[2] = {lt[0] > 0.0f ? sigma / lt[0] : 0.0f, lt[1] > 0.0f ? sigma / lt[1] : 0.0f};
     const float lse_r[2] = {lt[0] > 0.0f ? (m_ref[0] + log2f(lt[0])) * kLn2 : -INFINITY,
                             lt[1] > 0.0f ? (m_ref[1] + log2f(lt[1])) * kLn2 : -INFINITY};
     const int hs[2] = {h_lo, h_hi};
+    // Thread (g, c) holds, for head row r, dims 128w + 32c + 16e + 4q + i in
+    // o[4q + i][2r + e]: 32 contiguous output values per head row.
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
         const int h = hs[r];
         if (h >= H) continue;
-        const int i0 = 2 * r, i1 = 2 * r + 1;
         const float mm = mult[r];
         if (args.nsplit == 1) {
-            __nv_bfloat16* orow = args.out + (static_cast<int64_t>(t) * H + h) * kLatent + 128 * warp + 8 * c;
+            __nv_bfloat16* orow = args.out + (static_cast<int64_t>(t) * H + h) * kLatent + 128 * warp + 32 * c;
 #pragma unroll
-            for (int qd = 0; qd < 4; ++qd) {
-                uint4 v;
-                v.x = pack_bf16x2(o[4 * qd + 0][i0] * mm, o[4 * qd + 1][i0] * mm);
-                v.y = pack_bf16x2(o[4 * qd + 2][i0] * mm, o[4 * qd + 3][i0] * mm);
-                v.z = pack_bf16x2(o[4 * qd + 0][i1] * mm, o[4 * qd + 1][i1] * mm);
-                v.w = pack_bf16x2(o[4 * qd + 2][i1] * mm, o[4 * qd + 3][i1] * mm);
-                st_v4(orow + 32 * qd, v);
+            for (int e = 0; e < 2; ++e) {
+#pragma unroll
+                for (int hq = 0; hq < 2; ++hq) {
+                    uint4 v;
+                    v.x = pack_bf16x2(o[8 * hq + 0][2 * r + e] * mm, o[8 * hq + 1][2 * r + e] * mm);
+                    v.y = pack_bf16x2(o[8 * hq + 2][2 * r + e] * mm, o[8 * hq + 3][2 * r + e] * mm);
+                    v.z = pack_bf16x2(o[8 * hq + 4][2 * r + e] * mm, o[8 * hq + 5][2 * r + e] * mm);
+                    v.w = pack_bf16x2(o[8 * hq + 6][2 * r + e] * mm, o[8 * hq + 7][2 * r + e] * mm);
+                    st_v4(orow + 16 * e + 8 * hq, v);
+                }
             }
             if (warp == 0 && c == 0) args.lse[static_cast<int64_t>(t) * H + h] = lse_r[r];
         } else {
             const int64_t prow = (static_cast<int64_t>(t) * args.nsplit + split) * H + h;
-            float* orow = args.ws_o + prow * kLatent + 128 * warp + 8 * c;
+            float* orow = args.ws_o + prow * kLatent + 128 * warp + 32 * c;
 #pragma unroll
-            for (int qd = 0; qd < 4; ++qd) {
-                reinterpret_cast<float4*>(orow + 32 * qd)[0] =
-                    make_float4(o[4 * qd + 0][i0] * mm, o[4 * qd + 1][i0] * mm, o[4 * qd + 2][i0] * mm, o[4 * qd + 3][i0] * mm);
-                reinterpret_cast<float4*>(orow + 32 * qd)[1] =
-                    make_float4(o[4 * qd + 0][i1] * mm, o[4 * qd + 1][i1] * mm, o[4 * qd + 2][i1] * mm, o[4 * qd + 3][i1] * mm);
+            for (int e = 0; e < 2; ++e) {
+#pragma unroll
+                for (int qd = 0; qd < 4; ++qd)
+                    reinterpret_cast<float4*>(orow + 16 * e + 4 * qd)[0] =
+                        make_float4(o[4 * qd + 0][2 * r + e] * mm, o[4 * qd + 1][2 * r + e] * mm,
+                                    o[4 * qd + 2][2 * r + e] * mm, o[4 * qd + 3][2 * r + e] * mm);
             }
             if (warp == 0 && c == 0) args.ws_lse[prow] = lse_r[r];
         }
