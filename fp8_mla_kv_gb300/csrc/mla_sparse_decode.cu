@@ -556,13 +556,16 @@ mla_split_combine_kernel(const float* __restrict__ ws_o, const float* __restrict
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Number of splits of each token's top-k list: enough CTAs for about four per
-// SM, at least 64 positions per split, and at most kListMax positions per split.
+// Number of splits of each token's top-k list. A CTA's row rate is set by its
+// one copy-issuing warp, and a split costs a partial write, a merge and one more
+// prologue, so a token's list is split only when there are fewer (token, head
+// group) pairs than SMs; then into enough pieces for about two CTAs per SM,
+// each of at least 64 positions. At most kListMax positions per split.
 int choose_nsplit(int T, int H, int W, int sms) {
     if (T <= 0 || W <= 0) return 1;
     const int64_t base = static_cast<int64_t>(T) * ((H + kHeads - 1) / kHeads);
-    const int64_t target = 4ll * sms;
-    int64_t ns = (target + base - 1) / base;
+    int64_t ns = 1;
+    if (base < sms) ns = (2ll * sms + base - 1) / base;
     const int64_t max_ns = (W >= 64) ? W / 64 : 1;
     if (ns > max_ns) ns = max_ns;
     const int64_t min_ns = (W + kListMax - 1) / kListMax;
