@@ -152,9 +152,9 @@ WORKLOADS = {
               "8,192 rows (random 25% aimed at slot 0) then mla_sparse_decode T=256, H=16, d_qk=576, top-k "
               "2,048 all present, sm_scale=1/sqrt(576)"),
     # reduced case of the same kernels for ncu captures (cache 172 MB > L2)
-    "sweep-small": (lambda: workloads.sweep(num_slots=262144, T=64),
-                    "reduced sweep for profiling: 262,144-slot cache; 8,192-row padded write; decode T=64, "
-                    "H=16, top-k 2,048"),
+    "sweep-small": (lambda: workloads.sweep(num_slots=262144, T=256),
+                    "reduced sweep for profiling: 262,144-slot cache (172 MB); 8,192-row padded write; decode "
+                    "T=256, H=16, top-k 2,048 (the full sweep's launch shape)"),
     "nope": (lambda: workloads.nope(),
              "NoPE decode: 131,072-slot cache, T=64, H=16, d_qk=512, W=2,176, active length U(1..2048)"),
     "rope": (lambda: workloads.rope(),
