@@ -45,6 +45,20 @@ def dist_env():
     return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
 
 
+def max_over_ranks(values, world, device="cpu"):
+    """Element-wise maximum of per-rank totals: the slowest rank sets the job's time."""
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    if world > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return t.tolist()
+
+
+def job_rate(world, units_per_rank, seconds):
+    """Whole-job throughput under weak scaling: every rank processes the same units
+    in parallel, so the job does world * units_per_rank in the slowest rank's time."""
+    return world * units_per_rank / seconds
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -351,11 +365,8 @@ def run_ours(args, rank, world, local_rank):
         e2e_ms = [float("nan")]
 
     # reduce: max over ranks of the summed device time
-    tot = torch.tensor([sum(s_ms), sum(w_ms), sum(d_ms), sum(e2e_ms)], dtype=torch.float64, device=dev)
-    if world > 1:
-        torch.distributed.all_reduce(tot, op=torch.distributed.ReduceOp.MAX)
-    step_ms, writer_ms, decode_ms, e2e_tot = (tot / torch.tensor([K, K, K, len(e2e_ms)], device=dev,
-                                                                  dtype=torch.float64)).tolist()
+    tot = max_over_ranks([sum(s_ms), sum(w_ms), sum(d_ms), sum(e2e_ms)], world, dev)
+    step_ms, writer_ms, decode_ms, e2e_tot = (tot[0] / K, tot[1] / K, tot[2] / K, tot[3] / len(e2e_ms))
 
     n_valid = int(((db.topk > 0) & (db.topk < wl.num_slots)).sum())
     row_read = 656 if db.d_qk == 576 else 528
@@ -377,7 +388,7 @@ def run_ours(args, rank, world, local_rank):
             cpu = oracle_cpu_baseline(wl, cache_np, wb, seconds=args.cpu_seconds)
         result = {
             "metric": METRIC,
-            "value": world * db.T / (step_ms * 1e-3),
+            "value": job_rate(world, db.T, step_ms * 1e-3),
             "unit": UNIT,
             "n_gpus": world,
             "steps": K,
@@ -399,7 +410,7 @@ def run_ours(args, rank, world, local_rank):
             },
             "decode": {
                 "us": decode_ms * 1e3,
-                "query_tokens_per_s": world * db.T / (decode_ms * 1e-3),
+                "query_tokens_per_s": job_rate(world, db.T, decode_ms * 1e-3),
                 "gathered_kv_gbs": gathered / (decode_ms * 1e-3) / 1e9,
                 "gathered_bytes": gathered,
                 "nsplit_workspace_bytes": 0 if ws is None else int(ws.numel()),
@@ -410,7 +421,7 @@ def run_ours(args, rank, world, local_rank):
                 note="one call over every slot 1..N-1 (sequential slots), CUDA-graph replay, L2 flushed"),
             "writer": None if wb is None else {
                 "us": writer_ms * 1e3,
-                "rows_per_s": world * n_rows / (writer_ms * 1e-3),
+                "rows_per_s": job_rate(world, n_rows, writer_ms * 1e-3),
                 "algorithmic_gbs": writer_alg / (writer_ms * 1e-3) / 1e9,
                 "hbm_frac": writer_alg / (writer_ms * 1e-3) / 1e9 / peak,
             },
@@ -427,7 +438,7 @@ def run_ours(args, rank, world, local_rank):
             },
             "clocks": clocks,
             "e2e": {
-                "value": world * db.T / (e2e_tot * 1e-3),
+                "value": job_rate(world, db.T, e2e_tot * 1e-3),
                 "unit": UNIT,
                 "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
