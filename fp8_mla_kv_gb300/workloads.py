@@ -112,6 +112,8 @@ class Workload:
     decode: Optional[DecodeBatch]
     description: str = ""
     block_table: Optional[torch.Tensor] = None   # C4 only: physical page of each logical page
+    topk_logical: Optional[torch.Tensor] = None  # C4 only: the decode's top-k as sequence positions (-1 pad)
+    page_size: int = 0                           # C4 only: slots per page
 
     def cache_bytes(self) -> int:
         return self.num_slots * ROW_BYTES
@@ -209,14 +211,16 @@ def prefill(seed: int = 0, num_pages: int = 1024, page: int = 64, T: int = 1024,
     phys = table[pos // page] * page + pos % page
     q = _randn_bf16((T, H, LATENT + ROPE), seed, "prefill.q")
     topk = torch.full((T, W), -1, dtype=torch.int32)
+    logical = torch.full((T, W), -1, dtype=torch.int32)
     for i in range(T):
         k = min(i + 1, W)
         chosen = torch.randperm(i + 1, generator=g)[:k]
         topk[i, :k] = phys[chosen].to(torch.int32)
+        logical[i, :k] = chosen.to(torch.int32)
     return Workload("prefill", num_slots, 0xFF, fill, [],
                     DecodeBatch(q, topk, 1.0 / math.sqrt(576), "prefill"),
                     f"{num_slots}-slot cache in {num_pages} pages of {page}; T={T} causal rows; slot 0 = 0xFF",
-                    block_table=table)
+                    block_table=table, topk_logical=logical, page_size=page)
 
 
 def sweep(seed: int = 0, num_slots: int = 1048576, sizes=(1, 64, 1024, 8192), T: int = 256,

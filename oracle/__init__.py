@@ -16,6 +16,16 @@ Parity status (what pins each function to something other than itself):
     (with torch's fp8 table as the decoder) on tiny inputs, closed forms
     (single entry, q = 0, all-equal rows), permutation invariance and the
     zero-RoPE == NoPE identity.
+  * 528-byte rows (``kv_write`` / ``sparse_decode`` on a [N, 528] cache) -
+    pinned: each row equals the first 528 bytes of the 656-byte NoPE row, and
+    the decode over them equals the decode over the 656-byte NoPE cache.
+  * ``paged_to_physical`` - pinned against the prefill workload's generator,
+    which maps its positions to slots with its own code, and by the identity
+    block table.
+  * ``gather_upconvert`` - pinned: with power-of-two scales against torch's
+    float8_e4m3fn -> bfloat16 conversion; with arbitrary scales against an
+    exact rational nearest-BF16 search; RoPE tail bit-identical, NoPE tail and
+    absent rows zero.
 
 The arithmetic lives in ``mla_oracle.cpp`` (scalar C++17, float64 accumulation).
 """
@@ -34,7 +44,8 @@ _LIB = os.path.join(_HERE, "liboracle_mla.so")
 _lock = threading.Lock()
 _lib = None
 
-ROW_BYTES = 656  # restated from the row layout, not imported from the library
+ROW_BYTES = 656       # restated from the row layout, not imported from the library
+ROW_BYTES_NOPE = 528  # the canonical NoPE row: latent + scales, no tail
 
 
 def build(force: bool = False) -> str:
@@ -71,6 +82,19 @@ def _load():
                                                  c.c_void_p, c.c_int64, c.c_void_p, c.c_int,
                                                  c.c_float, c.c_void_p, c.c_void_p,
                                                  c.c_void_p, c.c_int, c.c_int]
+            lib.oracle_kv_write_rows.restype = c.c_int64
+            lib.oracle_kv_write_rows.argtypes = [c.c_void_p, c.c_int64, c.c_int64, c.c_void_p, c.c_void_p,
+                                                 c.c_void_p, c.c_int64, c.c_int64]
+            lib.oracle_sparse_decode_rows.restype = c.c_int64
+            lib.oracle_sparse_decode_rows.argtypes = [c.c_void_p, c.c_int, c.c_int, c.c_int,
+                                                      c.c_void_p, c.c_int64, c.c_int64, c.c_void_p, c.c_int,
+                                                      c.c_float, c.c_void_p, c.c_void_p,
+                                                      c.c_void_p, c.c_int, c.c_int]
+            lib.oracle_double_to_bf16.restype = c.c_uint16
+            lib.oracle_double_to_bf16.argtypes = [c.c_double]
+            lib.oracle_gather_upconvert.restype = c.c_int64
+            lib.oracle_gather_upconvert.argtypes = [c.c_void_p, c.c_int64, c.c_int64, c.c_void_p, c.c_int64,
+                                                    c.c_int, c.c_void_p]
             _lib = lib
     return _lib
 
@@ -117,12 +141,14 @@ def e4m3_encode_bit_range(lo: int, hi: int, n_threads: int | None = None) -> np.
 
 
 def kv_write(cache: np.ndarray, slot_idx, latent, rope, reserved_slot: int = 0) -> int:
-    """Write rows into ``cache`` (uint8 [num_slots, 656], modified in place).
+    """Write rows into ``cache`` (uint8 [num_slots, 656] or [num_slots, 528] for
+    NoPE-only rows; modified in place).
 
-    latent: bf16 [n, 512]; rope: bf16 [n, 64] or None (NoPE). Returns the number
-    of rows dropped for an out-of-range slot.
+    latent: bf16 [n, 512]; rope: bf16 [n, 64] or None (NoPE; required for 528-byte
+    rows). Returns the number of rows dropped for an out-of-range slot.
     """
-    assert cache.dtype == np.uint8 and cache.ndim == 2 and cache.shape[1] == ROW_BYTES
+    assert cache.dtype == np.uint8 and cache.ndim == 2 and cache.shape[1] in (ROW_BYTES, ROW_BYTES_NOPE)
+    assert rope is None or cache.shape[1] == ROW_BYTES
     assert cache.flags.c_contiguous
     slots = np.ascontiguousarray(np.asarray(slot_idx, dtype=np.int64))
     lat = _u16(latent)
@@ -132,8 +158,8 @@ def kv_write(cache: np.ndarray, slot_idx, latent, rope, reserved_slot: int = 0) 
     if rope is not None:
         rp = _u16(rope)
         assert rp.size == n * 64
-    return int(_load().oracle_kv_write(_ptr(cache), cache.shape[0], _ptr(slots), _ptr(lat),
-                                       _ptr(rp) if rp is not None else None, n, reserved_slot))
+    return int(_load().oracle_kv_write_rows(_ptr(cache), cache.shape[0], cache.shape[1], _ptr(slots), _ptr(lat),
+                                            _ptr(rp) if rp is not None else None, n, reserved_slot))
 
 
 def sparse_decode(q, cache: np.ndarray, topk, sm_scale: float, tokens=None,
@@ -150,7 +176,8 @@ def sparse_decode(q, cache: np.ndarray, topk, sm_scale: float, tokens=None,
     tk = np.ascontiguousarray(np.asarray(topk, dtype=np.int32))
     assert tk.shape[0] == T
     W = tk.shape[1]
-    assert cache.dtype == np.uint8 and cache.flags.c_contiguous and cache.shape[1] == ROW_BYTES
+    assert cache.dtype == np.uint8 and cache.flags.c_contiguous and cache.shape[1] in (ROW_BYTES, ROW_BYTES_NOPE)
+    assert cache.shape[1] == ROW_BYTES or d_qk == 512
     out = np.full((T, H, 512), np.nan, dtype=np.float64)
     lse = np.full((T, H), np.nan, dtype=np.float64)
     tok = None
@@ -158,8 +185,65 @@ def sparse_decode(q, cache: np.ndarray, topk, sm_scale: float, tokens=None,
     if tokens is not None:
         tok = np.ascontiguousarray(np.asarray(tokens, dtype=np.int32))
         n_tok = tok.size
-    bad = _load().oracle_sparse_decode(_ptr(qu), T, H, d_qk, _ptr(cache), cache.shape[0],
-                                       _ptr(tk), W, float(sm_scale), _ptr(out), _ptr(lse),
-                                       _ptr(tok) if tok is not None else None, n_tok,
-                                       n_threads or default_threads())
+    bad = _load().oracle_sparse_decode_rows(_ptr(qu), T, H, d_qk, _ptr(cache), cache.shape[0], cache.shape[1],
+                                            _ptr(tk), W, float(sm_scale), _ptr(out), _ptr(lse),
+                                            _ptr(tok) if tok is not None else None, n_tok,
+                                            n_threads or default_threads())
     return out, lse, int(bad)
+
+
+def paged_to_physical(topk_logical, block_table, page_size: int, token_seq=None):
+    """Physical slots of a top-k list given as sequence positions (vLLM PR #55277,
+    "Relation to #53969": the indexer's positions go through the block table).
+
+    topk_logical: int32 [T, W], -1 (any negative) = absent. block_table: int32
+    [n_seq, max_pages], the physical page of each logical page; a negative entry
+    is an unassigned page. token_seq: int32 [T], the block-table row of each token
+    (None: row 0 for every token). Position p of token t maps to slot
+    block_table[seq, p // page_size] * page_size + p % page_size. Returns (int32
+    [T, W] physical slots with -1 where absent, number of positions past the end
+    of the table, which are absent too).
+    """
+    lg = np.asarray(topk_logical, dtype=np.int64)
+    bt = np.asarray(block_table, dtype=np.int64)
+    if bt.ndim == 1:
+        bt = bt[None, :]
+    T, W = lg.shape
+    seq = np.zeros(T, dtype=np.int64) if token_seq is None else np.asarray(token_seq, dtype=np.int64)
+    out = np.full((T, W), -1, dtype=np.int64)
+    bad = 0
+    for t in range(T):
+        row = bt[seq[t]]
+        for j in range(W):
+            p = lg[t, j]
+            if p < 0:
+                continue
+            page = p // page_size
+            if page >= row.shape[0]:
+                bad += 1
+                continue
+            phys_page = row[page]
+            if phys_page < 0:
+                continue
+            out[t, j] = phys_page * page_size + p % page_size
+    return out.astype(np.int32), bad
+
+
+def double_to_bf16(x: float) -> int:
+    """BF16 bits of the value nearest to x (ties to even); NaN -> 0x7FC0."""
+    return int(_load().oracle_double_to_bf16(float(x)))
+
+
+def gather_upconvert(cache: np.ndarray, slots, pe_dim: int):
+    """Rows of ``cache`` at ``slots`` (int32 [n]) widened to BF16 [n, 576] (uint16
+    bits): the latent as the BF16 nearest to e4m3 * scale, then the RoPE tail
+    (pe_dim 64) or zeros (pe_dim 0). Absent slots (<= 0 or >= num_slots) give
+    zero rows. Returns (out, number of slots >= num_slots).
+    """
+    assert cache.dtype == np.uint8 and cache.flags.c_contiguous and cache.shape[1] in (ROW_BYTES, ROW_BYTES_NOPE)
+    assert pe_dim in (0, 64) and (cache.shape[1] == ROW_BYTES or pe_dim == 0)
+    sl = np.ascontiguousarray(np.asarray(slots, dtype=np.int32))
+    out = np.empty((sl.size, 576), dtype=np.uint16)
+    bad = _load().oracle_gather_upconvert(_ptr(cache), cache.shape[0], cache.shape[1], _ptr(sl), sl.size,
+                                          pe_dim, _ptr(out))
+    return out, int(bad)

@@ -19,6 +19,12 @@
 //   [sglang-39288] sglang PR #39288 "SM120 sparse MLA: zero-initialise the
 //                page-split scratch", Root cause: a masked (-1) top-k candidate
 //                must contribute nothing, whatever slot 0 holds.
+//   [sglang-39288] "Relation to other changes": the canonical NoPE row of
+//                flashinfer#5075 is 528 bytes (the 512-byte latent and the 16
+//                bytes of scales, no tail).
+//   [vLLM-55277] Changes table, cp_gather_and_upconvert_fp8_kv_cache: gathers
+//                rows of the cache and widens them to BF16 for the chunked-
+//                context path, the NoPE tail written as exact zeros.
 //   OCP 8-bit Floating Point Specification (OFP8), E4M3 format: bias 7,
 //                3 mantissa bits, no infinities, S.1111.111 is NaN, max finite
 //                448, subnormals m * 2^-9.
@@ -34,7 +40,11 @@
 //   * a decode entry is present iff 0 < idx < num_slots; -1 (any negative), the
 //     reserved slot 0 and out-of-range slots are absent and never read;
 //   * lse is the natural log of the sum of exp of the *scaled* scores;
-//     an empty entry set gives out = 0 and lse = -inf.
+//     an empty entry set gives out = 0 and lse = -inf;
+//   * a 528-byte row is the 656-byte row without its tail (NoPE only);
+//   * the upconverted latent value is the BF16 nearest to the exact product
+//     e4m3(byte) * scale (ties to even), NaN codes give 0x7FC0; an absent slot
+//     gives a row of zeros.
 
 #include <cmath>
 #include <cstdint>
@@ -46,8 +56,10 @@
 
 namespace {
 
-// Row layout, restated from [vLLM-55277] Purpose item 1.
+// Row layout, restated from [vLLM-55277] Purpose item 1 (656 bytes) and
+// [sglang-39288] "Relation to other changes" (528 bytes, no tail).
 constexpr int64_t kRowBytes = 656;
+constexpr int64_t kRowBytesNope = 528;
 constexpr int kLatent = 512;
 constexpr int kTileValues = 128;
 constexpr int kTiles = 4;
@@ -147,9 +159,12 @@ void oracle_e4m3_encode_bit_range(uint64_t lo, uint64_t hi, uint8_t* out, int n_
 // [sglang-47013] Summary / Motivation (drop rows aimed at the reserved slot).
 // Returns the number of rows whose slot was >= num_slots (dropped as well).
 // ---------------------------------------------------------------------------
-int64_t oracle_kv_write(uint8_t* cache, int64_t num_slots, const int64_t* slot_idx,
-                        const uint16_t* latent_bf16, const uint16_t* rope_bf16,
-                        int64_t n_rows, int64_t reserved_slot) {
+// row_bytes is 656 or 528; a 528-byte row has no tail, so rope must be null
+// (returns -1 otherwise).
+int64_t oracle_kv_write_rows(uint8_t* cache, int64_t num_slots, int64_t row_bytes, const int64_t* slot_idx,
+                             const uint16_t* latent_bf16, const uint16_t* rope_bf16,
+                             int64_t n_rows, int64_t reserved_slot) {
+    if (row_bytes != kRowBytes && !(row_bytes == kRowBytesNope && rope_bf16 == nullptr)) return -1;
     int64_t out_of_range = 0;
     for (int64_t r = 0; r < n_rows; ++r) {
         const int64_t slot = slot_idx[r];
@@ -157,7 +172,7 @@ int64_t oracle_kv_write(uint8_t* cache, int64_t num_slots, const int64_t* slot_i
         // dropped before any of their inputs is read.
         if (slot == reserved_slot || slot < 0) continue;
         if (slot >= num_slots) { ++out_of_range; continue; }
-        uint8_t* row = cache + slot * kRowBytes;
+        uint8_t* row = cache + slot * row_bytes;
         const uint16_t* x = latent_bf16 + r * kLatent;
         for (int t = 0; t < kTiles; ++t) {
             // Step 2: tile amax, ignoring every NaN (quiet or signaling: a bf16 NaN
@@ -180,7 +195,9 @@ int64_t oracle_kv_write(uint8_t* cache, int64_t num_slots, const int64_t* slot_i
             for (int k = 0; k < 4; ++k)
                 row[kScaleOffset + 4 * t + k] = static_cast<uint8_t>((sbits >> (8 * k)) & 0xFF);
         }
-        // Step 6: the tail: 64 bf16 RoPE values bit for bit, or 128 zero bytes.
+        // Step 6: the tail: 64 bf16 RoPE values bit for bit, or 128 zero bytes
+        // (a 528-byte row has none).
+        if (row_bytes == kRowBytesNope) continue;
         for (int k = 0; k < kRope; ++k) {
             const uint16_t v = rope_bf16 ? rope_bf16[r * kRope + k] : 0;
             row[kTailOffset + 2 * k] = static_cast<uint8_t>(v & 0xFF);
@@ -188,6 +205,13 @@ int64_t oracle_kv_write(uint8_t* cache, int64_t num_slots, const int64_t* slot_i
         }
     }
     return out_of_range;
+}
+
+int64_t oracle_kv_write(uint8_t* cache, int64_t num_slots, const int64_t* slot_idx,
+                        const uint16_t* latent_bf16, const uint16_t* rope_bf16,
+                        int64_t n_rows, int64_t reserved_slot) {
+    return oracle_kv_write_rows(cache, num_slots, kRowBytes, slot_idx, latent_bf16, rope_bf16, n_rows,
+                                reserved_slot);
 }
 
 // ---------------------------------------------------------------------------
@@ -203,11 +227,12 @@ int64_t oracle_kv_write(uint8_t* cache, int64_t num_slots, const int64_t* slot_i
 // all T tokens are computed. Outputs are written at the token's own row.
 // Returns the number of out-of-range (>= num_slots) entries seen.
 // ---------------------------------------------------------------------------
-int64_t oracle_sparse_decode(const uint16_t* q_bf16, int T, int H, int d_qk,
-                             const uint8_t* cache, int64_t num_slots,
-                             const int32_t* topk, int W, float sm_scale_f,
-                             double* out, double* lse,
-                             const int32_t* tokens, int n_tokens, int n_threads) {
+int64_t oracle_sparse_decode_rows(const uint16_t* q_bf16, int T, int H, int d_qk,
+                                  const uint8_t* cache, int64_t num_slots, int64_t row_bytes,
+                                  const int32_t* topk, int W, float sm_scale_f,
+                                  double* out, double* lse,
+                                  const int32_t* tokens, int n_tokens, int n_threads) {
+    if (row_bytes != kRowBytes && !(row_bytes == kRowBytesNope && d_qk == kLatent)) return -1;
     const double sm_scale = static_cast<double>(sm_scale_f);
     const bool with_rope = (d_qk == kLatent + kRope);
     const int n_work = tokens ? n_tokens : T;
@@ -228,7 +253,7 @@ int64_t oracle_sparse_decode(const uint16_t* q_bf16, int T, int H, int d_qk,
                 const int64_t idx = topk[static_cast<int64_t>(t) * W + j];
                 if (idx <= 0) continue;
                 if (idx >= num_slots) { ++local_bad; continue; }
-                const uint8_t* row = cache + idx * kRowBytes;
+                const uint8_t* row = cache + idx * row_bytes;
                 for (int tt = 0; tt < kTiles; ++tt) {
                     uint32_t sbits = 0;
                     for (int k = 0; k < 4; ++k)
@@ -286,6 +311,81 @@ int64_t oracle_sparse_decode(const uint16_t* q_bf16, int T, int H, int d_qk,
     worker();
     for (auto& th : pool) th.join();
     return bad.load();
+}
+
+int64_t oracle_sparse_decode(const uint16_t* q_bf16, int T, int H, int d_qk,
+                             const uint8_t* cache, int64_t num_slots,
+                             const int32_t* topk, int W, float sm_scale_f,
+                             double* out, double* lse,
+                             const int32_t* tokens, int n_tokens, int n_threads) {
+    return oracle_sparse_decode_rows(q_bf16, T, H, d_qk, cache, num_slots, kRowBytes, topk, W, sm_scale_f,
+                                     out, lse, tokens, n_tokens, n_threads);
+}
+
+// ---------------------------------------------------------------------------
+// Gather and upconvert ([vLLM-55277] Changes table, cp_gather_and_upconvert_
+// fp8_kv_cache): out[i, 0:512] = BF16 nearest to e4m3(byte_d) * scale_{d/128}
+// for the row at slots[i]; out[i, 512:576] = the 64 BF16 RoPE values of the
+// tail when pe_dim == 64, zeros when pe_dim == 0 (the tail is not read). An
+// absent slot (<= 0, or >= num_slots, counted) gives a row of zeros.
+// Returns the number of slots >= num_slots.
+// ---------------------------------------------------------------------------
+
+// BF16 bits of the value nearest to x, ties to even (x is the exact product, a
+// double); NaN -> 0x7FC0. BF16 has 8 significant bits and fp32's exponent range:
+// normal quantum 2^(e-7) for 2^e <= |x| < 2^(e+1), e >= -126; below 2^-126 the
+// quantum is 2^-133.
+uint16_t oracle_double_to_bf16(double x) {
+    if (std::isnan(x)) return 0x7FC0;
+    const double a = std::fabs(x);
+    double r;
+    if (a == 0.0) {
+        r = 0.0;
+    } else {
+        int ex;
+        std::frexp(a, &ex);                          // a = f * 2^ex, f in [0.5, 1)
+        const int e = ex - 1;                        // floor(log2 a)
+        const int q_exp = (e < -126) ? -133 : (e - 7);
+        r = std::ldexp(std::nearbyint(std::ldexp(a, -q_exp)), q_exp);   // ties to even
+    }
+    if (r > 3.3895313892515355e38) r = std::numeric_limits<double>::infinity();   // past the largest BF16
+    float f = static_cast<float>(std::signbit(x) ? -r : r);     // exact: r is a BF16 value
+    uint32_t u;
+    std::memcpy(&u, &f, sizeof u);
+    return static_cast<uint16_t>(u >> 16);
+}
+
+int64_t oracle_gather_upconvert(const uint8_t* cache, int64_t num_slots, int64_t row_bytes,
+                                const int32_t* slots, int64_t n, int pe_dim, uint16_t* out) {
+    if (row_bytes != kRowBytes && !(row_bytes == kRowBytesNope && pe_dim == 0)) return -1;
+    if (pe_dim != 0 && pe_dim != kRope) return -1;
+    int64_t bad = 0;
+    for (int64_t i = 0; i < n; ++i) {
+        uint16_t* o = out + i * (kLatent + kRope);
+        const int64_t idx = slots[i];
+        if (idx <= 0 || idx >= num_slots) {
+            if (idx >= num_slots) ++bad;
+            for (int d = 0; d < kLatent + kRope; ++d) o[d] = 0;
+            continue;
+        }
+        const uint8_t* row = cache + idx * row_bytes;
+        for (int t = 0; t < kTiles; ++t) {
+            uint32_t sbits = 0;
+            for (int k = 0; k < 4; ++k) sbits |= static_cast<uint32_t>(row[kScaleOffset + 4 * t + k]) << (8 * k);
+            float sc;
+            std::memcpy(&sc, &sbits, sizeof sc);
+            for (int v = 0; v < kTileValues; ++v) {
+                // 4 significant bits times 24: the product is exact in a double.
+                const double prod = oracle_e4m3_decode(row[t * kTileValues + v]) * static_cast<double>(sc);
+                o[t * kTileValues + v] = oracle_double_to_bf16(prod);
+            }
+        }
+        for (int k = 0; k < kRope; ++k)
+            o[kLatent + k] = (pe_dim == kRope)
+                ? static_cast<uint16_t>(row[kTailOffset + 2 * k] | (row[kTailOffset + 2 * k + 1] << 8))
+                : static_cast<uint16_t>(0);
+    }
+    return bad;
 }
 
 }  // extern "C"
