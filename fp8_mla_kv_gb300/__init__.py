@@ -7,5 +7,6 @@ use, and every call fails loudly if it is missing: there is no CPU fallback.
 """
 
 ROW_BYTES = 656
+ROW_BYTES_NOPE = 528
 LATENT_DIM = 512
 ROPE_DIM = 64

@@ -5,6 +5,9 @@
 // PR #47013 (Summary / Modifications: rows aimed at the reserved slot are
 // dropped; Motivation: the quantiser keeps BF16 NaNs).
 //
+// Rows are 656 bytes, or 528 for the canonical NoPE row without a tail
+// (sglang PR #39288, "Relation to other changes": flashinfer#5075).
+//
 // One warp per row. Lane l owns latent values 16l .. 16l+15 (two 16-byte
 // loads), so tile t = lanes 8t .. 8t+7 and the tile amax is a 3-step xor
 // shuffle. The 512 FP8 bytes leave in one fully coalesced 16-byte store per
@@ -29,7 +32,7 @@ __device__ __forceinline__ uint32_t quant2(float x0, float x1, float scale, floa
 }
 
 __global__ void __launch_bounds__(kWriterThreads)
-mla_kv_write_kernel(uint8_t* __restrict__ cache, int64_t num_slots,
+mla_kv_write_kernel(uint8_t* __restrict__ cache, int64_t num_slots, int64_t row_bytes,
                     const int64_t* __restrict__ slot_idx,
                     const uint16_t* __restrict__ latent,
                     const uint16_t* __restrict__ rope,
@@ -74,14 +77,14 @@ mla_kv_write_kernel(uint8_t* __restrict__ cache, int64_t num_slots,
             qv[k] = quant2(v[4 * k], v[4 * k + 1], scale, rcp, fast) |
                     (quant2(v[4 * k + 2], v[4 * k + 3], scale, rcp, fast) << 16);
 
-        uint8_t* row = cache + slot * static_cast<int64_t>(kRowBytes);
+        uint8_t* row = cache + slot * row_bytes;
         st_v4(row + 16 * lane, make_uint4(qv[0], qv[1], qv[2], qv[3]));
         const float s0 = __shfl_sync(0xffffffffu, scale, 0);
         const float s1 = __shfl_sync(0xffffffffu, scale, 8);
         const float s2 = __shfl_sync(0xffffffffu, scale, 16);
         const float s3 = __shfl_sync(0xffffffffu, scale, 24);
         if (lane < 8) {
-            st_v4(row + kTailOff + 16 * lane, tail);
+            if (row_bytes == kRowBytes) st_v4(row + kTailOff + 16 * lane, tail);
         } else if (lane == 8) {
             st_v4(row + kScaleOff, make_uint4(__float_as_uint(s0), __float_as_uint(s1),
                                               __float_as_uint(s2), __float_as_uint(s3)));
@@ -95,7 +98,9 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 extern "C" int mla_kv_write(mla_kv_cache_t kv, const int64_t* slot_idx, const void* latent_bf16,
                             const void* rope_bf16, int64_t n_rows, int64_t reserved_slot, void* stream) {
-    if (n_rows < 0 || kv.row_bytes != MLA_ROW_BYTES || kv.num_slots < 0) return MLA_EINVAL;
+    if (n_rows < 0 || kv.num_slots < 0) return MLA_EINVAL;
+    if (kv.row_bytes != MLA_ROW_BYTES && !(kv.row_bytes == MLA_ROW_BYTES_NOPE && rope_bf16 == nullptr))
+        return MLA_EINVAL;
     if (n_rows == 0) return MLA_OK;
     if (kv.data == nullptr || slot_idx == nullptr || latent_bf16 == nullptr) return MLA_EINVAL;
     if (!aligned16(kv.data) || !aligned16(latent_bf16) || (rope_bf16 && !aligned16(rope_bf16)) ||
@@ -109,7 +114,7 @@ extern "C" int mla_kv_write(mla_kv_cache_t kv, const int64_t* slot_idx, const vo
     const int64_t max_blocks = static_cast<int64_t>(sms) * 8;     // 64 resident warps per SM
     if (blocks > max_blocks) blocks = max_blocks;
     mla_kv_write_kernel<<<static_cast<unsigned>(blocks), kWriterThreads, 0, static_cast<cudaStream_t>(stream)>>>(
-        static_cast<uint8_t*>(kv.data), kv.num_slots, slot_idx, static_cast<const uint16_t*>(latent_bf16),
+        static_cast<uint8_t*>(kv.data), kv.num_slots, kv.row_bytes, slot_idx, static_cast<const uint16_t*>(latent_bf16),
         static_cast<const uint16_t*>(rope_bf16), n_rows, reserved_slot, err);
     return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ECUDA;
 }

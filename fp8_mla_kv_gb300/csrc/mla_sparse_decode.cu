@@ -33,6 +33,7 @@
 // Splits write a normalised partial (o, lse) to the caller's workspace and a
 // second kernel merges them in split order (deterministic: no float atomics).
 #include <cfloat>
+#include <climits>
 #include <cmath>
 
 #include "mla_device.cuh"
@@ -79,6 +80,12 @@ struct DecodeArgs {
     float* ws_lse;    // [T, nsplit, H]
     int* err;
     int64_t num_slots;
+    int64_t row_bytes;          // 656, or 528 (NoPE rows without a tail)
+    // Paged top-k (page_size > 0): entries are sequence positions, mapped to
+    // slots through block_table[seq][position / page_size].
+    const int32_t* block_table; // [n_seq, bt_pages]
+    const int32_t* token_seq;   // [T] block-table row of each token, or null (row 0)
+    int bt_pages, n_seq, page_size;
     int T, H, d_qk, W, nsplit, split_len;
     float sm_scale_log2;   // sm_scale * log2(e)
 };
@@ -156,6 +163,28 @@ mla_sparse_decode_kernel(const DecodeArgs args) {
     int idxv[kPerThread];
 #pragma unroll
     for (int k = 0; k < kPerThread; ++k) idxv[k] = (k < mine) ? __ldg(trow + k) : -1;
+    if (args.page_size > 0) {
+        // Positions -> slots (vLLM PR #55277, "Relation to #53969"): a negative
+        // position or an unassigned (negative) page is absent; a position past
+        // the table is absent and flagged.
+        const int sq = args.token_seq ? __ldg(args.token_seq + t) : 0;
+        const bool seq_ok = sq >= 0 && sq < args.n_seq;
+        const int32_t* bt = args.block_table + static_cast<int64_t>(seq_ok ? sq : 0) * args.bt_pages;
+#pragma unroll
+        for (int k = 0; k < kPerThread; ++k) {
+            const int pos = idxv[k];
+            if (pos < 0) continue;
+            const int page = pos / args.page_size;
+            if (!seq_ok || page >= args.bt_pages) {
+                atomicOr(args.err, MLA_ERR_DECODE_INDEX_RANGE);
+                idxv[k] = -1;
+                continue;
+            }
+            const int phys = __ldg(bt + page);
+            const int64_t slot = static_cast<int64_t>(phys) * args.page_size + (pos - page * args.page_size);
+            idxv[k] = (phys < 0) ? -1 : static_cast<int>(min(slot, static_cast<int64_t>(INT32_MAX)));
+        }
+    }
     int cnt = 0;
 #pragma unroll
     for (int k = 0; k < kPerThread; ++k) {
@@ -211,7 +240,7 @@ mla_sparse_decode_kernel(const DecodeArgs args) {
             __syncwarp();
             if (lane < n_b)
                 bulk_g2s(dst + lane * kRowBytes,
-                         args.cache + static_cast<int64_t>(list[b * kNB + lane]) * kRowBytes, kRowRead, &full[s]);
+                         args.cache + static_cast<int64_t>(list[b * kNB + lane]) * args.row_bytes, kRowRead, &full[s]);
         }
         if (lane == 0) *issued_s = b;
         __syncthreads();     // matches the consumers' final barrier
@@ -590,12 +619,21 @@ extern "C" size_t mla_sparse_decode_workspace_bytes(int T, int H, int W) {
     return workspace_for(T, H, choose_nsplit(T, H, W, sms));
 }
 
-extern "C" int mla_sparse_decode(const void* q_bf16, int T, int H, int d_qk, mla_kv_cache_t kv,
-                                 const int32_t* topk_idx, int W, float sm_scale, void* out_bf16,
-                                 float* lse, void* workspace, size_t workspace_bytes, void* stream) {
-    if (T < 0 || W < 0 || kv.row_bytes != MLA_ROW_BYTES || kv.num_slots < 0 || !std::isfinite(sm_scale))
-        return MLA_EINVAL;
+namespace {
+
+struct PageArgs {
+    const int32_t* block_table;
+    const int32_t* token_seq;
+    int bt_pages, n_seq, page_size;
+};
+
+int launch_decode(const void* q_bf16, int T, int H, int d_qk, mla_kv_cache_t kv, const int32_t* topk_idx,
+                  int W, float sm_scale, void* out_bf16, float* lse, void* workspace, size_t workspace_bytes,
+                  void* stream, const PageArgs& pg) {
+    if (T < 0 || W < 0 || kv.num_slots < 0 || !std::isfinite(sm_scale)) return MLA_EINVAL;
+    if (kv.row_bytes != MLA_ROW_BYTES && kv.row_bytes != MLA_ROW_BYTES_NOPE) return MLA_EINVAL;
     if (d_qk != kLatent && d_qk != kLatent + kRope) return MLA_EUNSUPPORTED;
+    if (kv.row_bytes == MLA_ROW_BYTES_NOPE && d_qk != kLatent) return MLA_EUNSUPPORTED;   // no tail to read
     if (H < 1 || H > 128) return MLA_EUNSUPPORTED;
     if (T == 0) return MLA_OK;
     if (q_bf16 == nullptr || out_bf16 == nullptr || lse == nullptr || (W > 0 && topk_idx == nullptr) ||
@@ -635,6 +673,12 @@ extern "C" int mla_sparse_decode(const void* q_bf16, int T, int H, int d_qk, mla
                           : nullptr;
     a.err = err;
     a.num_slots = kv.num_slots;
+    a.row_bytes = kv.row_bytes;
+    a.block_table = pg.block_table;
+    a.token_seq = pg.token_seq;
+    a.bt_pages = pg.bt_pages;
+    a.n_seq = pg.n_seq;
+    a.page_size = pg.page_size;
     a.T = T; a.H = H; a.d_qk = d_qk; a.W = W; a.nsplit = nsplit;
     a.split_len = (W + nsplit - 1) / nsplit;
     a.sm_scale_log2 = sm_scale * kLog2e;
@@ -651,4 +695,27 @@ extern "C" int mla_sparse_decode(const void* q_bf16, int T, int H, int d_qk, mla
         if (cudaGetLastError() != cudaSuccess) return MLA_ECUDA;
     }
     return MLA_OK;
+}
+
+}  // namespace
+
+extern "C" int mla_sparse_decode(const void* q_bf16, int T, int H, int d_qk, mla_kv_cache_t kv,
+                                 const int32_t* topk_idx, int W, float sm_scale, void* out_bf16,
+                                 float* lse, void* workspace, size_t workspace_bytes, void* stream) {
+    const PageArgs none{nullptr, nullptr, 0, 0, 0};
+    return launch_decode(q_bf16, T, H, d_qk, kv, topk_idx, W, sm_scale, out_bf16, lse, workspace, workspace_bytes,
+                         stream, none);
+}
+
+extern "C" int mla_sparse_decode_paged(const void* q_bf16, int T, int H, int d_qk, mla_kv_cache_t kv,
+                                       const int32_t* topk_pos, int W, const int32_t* block_table, int n_seq,
+                                       int max_pages, const int32_t* token_seq, int page_size, float sm_scale,
+                                       void* out_bf16, float* lse, void* workspace, size_t workspace_bytes,
+                                       void* stream) {
+    if (page_size <= 0 || max_pages <= 0 || n_seq <= 0 || block_table == nullptr ||
+        (reinterpret_cast<uintptr_t>(block_table) & 3u) || (reinterpret_cast<uintptr_t>(token_seq) & 3u))
+        return MLA_EINVAL;
+    const PageArgs pg{block_table, token_seq, max_pages, n_seq, page_size};
+    return launch_decode(q_bf16, T, H, d_qk, kv, topk_pos, W, sm_scale, out_bf16, lse, workspace, workspace_bytes,
+                         stream, pg);
 }

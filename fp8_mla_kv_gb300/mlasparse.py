@@ -13,7 +13,7 @@ import threading
 
 import torch
 
-from . import ROW_BYTES
+from . import ROW_BYTES, ROW_BYTES_NOPE
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libmlasparse.so")
@@ -26,9 +26,10 @@ MLA_ECUDA = -4
 MLA_ERR_WRITE_SLOT_RANGE = 0x1
 MLA_ERR_DECODE_INDEX_RANGE = 0x2
 MLA_ERR_PIPELINE_TIMEOUT = 0x4
+MLA_ERR_GATHER_INDEX_RANGE = 0x8
 
 SYMBOLS = ("mla_kv_write", "mla_sparse_decode", "mla_sparse_decode_workspace_bytes",
-           "mla_get_error", "mla_strerror")
+           "mla_sparse_decode_paged", "mla_gather_upconvert", "mla_get_error", "mla_strerror")
 
 
 class MlaError(RuntimeError):
@@ -64,6 +65,13 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
             lib.mla_sparse_decode.argtypes = [c.c_void_p, c.c_int, c.c_int, c.c_int, KVCache, c.c_void_p,
                                               c.c_int, c.c_float, c.c_void_p, c.c_void_p, c.c_void_p,
                                               c.c_size_t, c.c_void_p]
+            lib.mla_sparse_decode_paged.restype = c.c_int
+            lib.mla_sparse_decode_paged.argtypes = [c.c_void_p, c.c_int, c.c_int, c.c_int, KVCache, c.c_void_p,
+                                                    c.c_int, c.c_void_p, c.c_int, c.c_int, c.c_void_p, c.c_int,
+                                                    c.c_float, c.c_void_p, c.c_void_p, c.c_void_p, c.c_size_t,
+                                                    c.c_void_p]
+            lib.mla_gather_upconvert.restype = c.c_int
+            lib.mla_gather_upconvert.argtypes = [KVCache, c.c_void_p, c.c_int64, c.c_int, c.c_void_p, c.c_void_p]
             lib.mla_get_error.restype = c.c_int
             lib.mla_get_error.argtypes = [c.POINTER(c.c_int32)]
             lib.mla_strerror.restype = c.c_char_p
@@ -92,10 +100,12 @@ def _stream(stream) -> int:
 
 
 def kv_cache(cache: torch.Tensor) -> KVCache:
-    """View a uint8 [num_slots, 656] device tensor as the C cache descriptor."""
-    if cache.dtype != torch.uint8 or cache.dim() != 2 or cache.shape[1] != ROW_BYTES or not cache.is_contiguous():
-        raise ValueError("cache must be a contiguous uint8 tensor [num_slots, 656]")
-    return KVCache(cache.data_ptr(), cache.shape[0], ROW_BYTES)
+    """View a uint8 [num_slots, 656] (or [num_slots, 528] NoPE-only) device tensor
+    as the C cache descriptor."""
+    if (cache.dtype != torch.uint8 or cache.dim() != 2 or cache.shape[1] not in (ROW_BYTES, ROW_BYTES_NOPE)
+            or not cache.is_contiguous()):
+        raise ValueError("cache must be a contiguous uint8 tensor [num_slots, 656] or [num_slots, 528]")
+    return KVCache(cache.data_ptr(), cache.shape[0], int(cache.shape[1]))
 
 
 def mla_kv_write(cache: torch.Tensor, slot_idx: torch.Tensor, latent: torch.Tensor,
@@ -147,6 +157,56 @@ def mla_sparse_decode(q: torch.Tensor, cache: torch.Tensor, topk_idx: torch.Tens
     if rc != MLA_OK:
         raise MlaError(rc, "mla_sparse_decode")
     return out, lse
+
+
+def mla_sparse_decode_paged(q: torch.Tensor, cache: torch.Tensor, topk_pos: torch.Tensor,
+                            block_table: torch.Tensor, page_size: int, sm_scale: float,
+                            token_seq: torch.Tensor | None = None, out: torch.Tensor | None = None,
+                            lse: torch.Tensor | None = None, workspace: torch.Tensor | None = None, stream=None):
+    """Decode with the top-k given as sequence positions: q bf16 [T, H, d_qk]; topk_pos
+    int32 [T, W]; block_table int32 [n_seq, max_pages] (or [max_pages]); token_seq int32
+    [T] or None. Returns (out bf16 [T, H, 512], lse fp32 [T, H])."""
+    _require_cuda(q, cache, topk_pos, block_table, token_seq)
+    T, H, d_qk = (int(s) for s in q.shape)
+    W = int(topk_pos.shape[1])
+    bt = block_table if block_table.dim() == 2 else block_table.view(1, -1)
+    assert q.dtype == torch.bfloat16 and q.is_contiguous()
+    assert topk_pos.dtype == torch.int32 and topk_pos.is_contiguous() and topk_pos.shape[0] == T
+    assert bt.dtype == torch.int32 and bt.is_contiguous()
+    if token_seq is not None:
+        assert token_seq.dtype == torch.int32 and token_seq.is_contiguous() and token_seq.numel() == T
+    if out is None:
+        out = torch.empty((T, H, 512), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((T, H), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = alloc_workspace(T, H, W, q.device)
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_n = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    rc = load().mla_sparse_decode_paged(q.data_ptr(), T, H, d_qk, kv_cache(cache), topk_pos.data_ptr(), W,
+                                        bt.data_ptr(), int(bt.shape[0]), int(bt.shape[1]),
+                                        token_seq.data_ptr() if token_seq is not None else None, int(page_size),
+                                        float(sm_scale), out.data_ptr(), lse.data_ptr(), ws_ptr, ws_n,
+                                        _stream(stream))
+    if rc != MLA_OK:
+        raise MlaError(rc, "mla_sparse_decode_paged")
+    return out, lse
+
+
+def mla_gather_upconvert(cache: torch.Tensor, slots: torch.Tensor, pe_dim: int,
+                         out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Rows at slots (int32 [n]) widened to bf16 [n, 576]."""
+    _require_cuda(cache, slots, out)
+    n = int(slots.numel())
+    assert slots.dtype == torch.int32 and slots.is_contiguous()
+    if out is None:
+        out = torch.empty((n, 576), dtype=torch.bfloat16, device=cache.device)
+    assert out.dtype == torch.bfloat16 and out.is_contiguous() and out.numel() == n * 576
+    rc = load().mla_gather_upconvert(kv_cache(cache), slots.data_ptr(), n, int(pe_dim), out.data_ptr(),
+                                     _stream(stream))
+    if rc != MLA_OK:
+        raise MlaError(rc, "mla_gather_upconvert")
+    return out
 
 
 def mla_get_error() -> int:

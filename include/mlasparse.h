@@ -46,6 +46,9 @@ extern "C" {
 #define MLA_TAIL_OFFSET    528
 #define MLA_ROPE_DIM       64
 #define MLA_FP8_MAX        448.0f   /* largest finite E4M3 value */
+/* The canonical NoPE row of flashinfer#5075 (sglang PR #39288, "Relation to
+ * other changes"): the 656-byte row without its 128-byte tail. */
+#define MLA_ROW_BYTES_NOPE 528
 
 /* ---- return codes ---- */
 #define MLA_OK             0
@@ -58,9 +61,13 @@ extern "C" {
 #define MLA_ERR_WRITE_SLOT_RANGE   0x1  /* mla_kv_write: slot >= num_slots, row dropped */
 #define MLA_ERR_DECODE_INDEX_RANGE 0x2  /* mla_sparse_decode: index >= num_slots, entry absent */
 #define MLA_ERR_PIPELINE_TIMEOUT   0x4  /* a kernel's bounded wait on its own copies ran out */
+#define MLA_ERR_GATHER_INDEX_RANGE 0x8  /* mla_gather_upconvert: slot >= num_slots, zero row */
 
 /* A cache: `data` is a device array of num_slots rows of row_bytes bytes,
- * 16-byte aligned. row_bytes must be MLA_ROW_BYTES. */
+ * 16-byte aligned. row_bytes is MLA_ROW_BYTES (656), or MLA_ROW_BYTES_NOPE
+ * (528) for a cache of NoPE rows only: latent and scales at the same offsets,
+ * no tail. A 528-byte cache takes only NoPE calls (rope_bf16 NULL, d_qk 512,
+ * pe_dim 0); others return MLA_EINVAL or MLA_EUNSUPPORTED. */
 typedef struct {
     void*   data;
     int64_t num_slots;
@@ -85,11 +92,12 @@ typedef struct {
  *       byte    = e4m3 round-to-nearest-even, saturating to +-448, of x / scale_t
  *                 (IEEE fp32 division; a NaN x gives the NaN code 0x7F),
  *     the four scales go to bytes 512..527, and bytes 528..655 receive rope row r
- *     verbatim, or zeros when rope_bf16 is NULL.
+ *     verbatim, or zeros when rope_bf16 is NULL (a 528-byte row has no tail).
  * No other byte of the cache is touched.
  *
  * Arguments:
- *   kv            cache (device, 16-byte aligned, row_bytes == 656)
+ *   kv            cache (device, 16-byte aligned, row_bytes 656, or 528 with
+ *                 rope_bf16 NULL)
  *   slot_idx      int64 [n_rows], device
  *   latent_bf16   bf16 [n_rows, 512] row-major, device, 16-byte aligned
  *   rope_bf16     bf16 [n_rows, 64] row-major, device, 16-byte aligned; or NULL
@@ -137,7 +145,7 @@ size_t mla_sparse_decode_workspace_bytes(int T, int H, int W);
  *   q_bf16     bf16 [T, H, d_qk] row-major, device, 16-byte aligned
  *   T, H       tokens (>= 0; 0 launches nothing) and heads (1..128)
  *   d_qk       576 (512 latent + 64 RoPE) or 512 (NoPE: the row tail is not read)
- *   kv         the cache (row_bytes == 656, 16-byte aligned)
+ *   kv         the cache (16-byte aligned; row_bytes 656, or 528 with d_qk 512)
  *   topk_idx   int32 [T, W] row-major, device; W >= 0
  *   sm_scale   softmax scale applied to q . k (finite)
  *   out_bf16   bf16 [T, H, 512] row-major, device, 16-byte aligned
@@ -150,6 +158,58 @@ size_t mla_sparse_decode_workspace_bytes(int T, int H, int W);
 int mla_sparse_decode(const void* q_bf16, int T, int H, int d_qk, mla_kv_cache_t kv,
                       const int32_t* topk_idx, int W, float sm_scale, void* out_bf16,
                       float* lse, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * mla_sparse_decode_paged - mla_sparse_decode with the top-k list given as
+ * sequence positions and a block table (vLLM PR #55277, "Relation to #53969":
+ * the indexer emits logical positions that the kernel maps to cache slots).
+ *
+ * Entry j of token t is position p = topk_pos[t,j] of the token's sequence
+ * s = token_seq[t] (every token uses row 0 when token_seq is NULL). It stands for
+ * the slot  block_table[s, p / page_size] * page_size + p % page_size,  and
+ * the decode is then exactly mla_sparse_decode over those slots. A negative
+ * position or a negative (unassigned) block-table entry is absent; a page past
+ * max_pages, a sequence outside [0, n_seq) or a slot >= num_slots is absent and
+ * sets MLA_ERR_DECODE_INDEX_RANGE. Slot 0 stays absent.
+ *
+ * Arguments as mla_sparse_decode, plus:
+ *   topk_pos     int32 [T, W] positions, device
+ *   block_table  int32 [n_seq, max_pages] physical page of each logical page,
+ *                device, 4-byte aligned
+ *   token_seq    int32 [T] block-table row of each token, device, or NULL
+ *   page_size    slots per page (> 0)
+ * The workspace is mla_sparse_decode_workspace_bytes(T, H, W).
+ */
+int mla_sparse_decode_paged(const void* q_bf16, int T, int H, int d_qk, mla_kv_cache_t kv,
+                            const int32_t* topk_pos, int W, const int32_t* block_table, int n_seq,
+                            int max_pages, const int32_t* token_seq, int page_size, float sm_scale,
+                            void* out_bf16, float* lse, void* workspace, size_t workspace_bytes,
+                            void* stream);
+
+/*
+ * mla_gather_upconvert - gather rows of the cache and widen them to BF16
+ * (vLLM PR #55277, Changes table: cp_gather_and_upconvert_fp8_kv_cache, the
+ * chunked-context path; the NoPE tail is written as exact zeros).
+ *
+ * For i < n with s = slots[i]:
+ *   out[i, d]       = the BF16 value nearest to e4m3(byte_d) * scale[d / 128]
+ *                     (the exact product, rounded once, ties to even; a NaN
+ *                     code gives 0x7FC0),                         d < 512
+ *   out[i, 512 + k] = the RoPE value k of the row's tail (pe_dim 64), or 0
+ *                     (pe_dim 0: the tail is not read),           k < 64
+ * An absent slot (s <= 0) gives a row of zeros; s >= num_slots as well, and
+ * sets MLA_ERR_GATHER_INDEX_RANGE.
+ *
+ * Arguments:
+ *   kv        the cache (16-byte aligned; row_bytes 656, or 528 with pe_dim 0)
+ *   slots     int32 [n], device, 4-byte aligned
+ *   n         >= 0 (0 launches nothing)
+ *   pe_dim    64 or 0
+ *   out_bf16  bf16 [n, 576] row-major, device, 16-byte aligned
+ * Returns MLA_OK, MLA_EINVAL or MLA_ECUDA.
+ */
+int mla_gather_upconvert(mla_kv_cache_t kv, const int32_t* slots, int64_t n, int pe_dim,
+                         void* out_bf16, void* stream);
 
 /*
  * mla_sparse_decode_noalloc - mla_sparse_decode for callers that cannot

@@ -53,5 +53,19 @@ def test_host_validation_without_gpu(lib):
     assert lib.mla_sparse_decode(None, 0, 16, 576, kv, None, 8, 0.1, None, None, None, 0, None) == M.MLA_OK
     assert lib.mla_sparse_decode(None, 2, 16, 576, kv, None, 8, 0.1, None, None, None, 0, None) == M.MLA_EINVAL
     assert lib.mla_sparse_decode_workspace_bytes(0, 16, 8) == 0
+    # 528-byte rows take NoPE calls only
+    kv528 = M.KVCache(None, 16, 528)
+    rope = ctypes.c_void_p(16)
+    assert lib.mla_kv_write(kv528, None, None, rope, 3, 0, None) == M.MLA_EINVAL
+    assert lib.mla_sparse_decode(None, 1, 16, 576, kv528, None, 8, 0.1, None, None, None, 0, None) == M.MLA_EUNSUPPORTED
+    assert lib.mla_gather_upconvert(kv528, None, 4, 64, None, None) == M.MLA_EINVAL
+    # gather-and-upconvert: bad pe_dim, empty call, null pointers
+    assert lib.mla_gather_upconvert(kv, None, 4, 32, None, None) == M.MLA_EINVAL
+    assert lib.mla_gather_upconvert(kv, None, 0, 64, None, None) == M.MLA_OK
+    assert lib.mla_gather_upconvert(kv, None, 4, 64, None, None) == M.MLA_EINVAL
+    # paged decode: page size, table and sequence count are checked first
+    for ps, bt, nseq, mp in ((0, 16, 1, 4), (64, None, 1, 4), (64, 16, 0, 4), (64, 16, 1, 0)):
+        assert lib.mla_sparse_decode_paged(None, 1, 16, 576, kv, None, 8, bt, nseq, mp, None, ps, 0.1,
+                                           None, None, None, 0, None) == M.MLA_EINVAL
     for code in (0, -1, -2, -3, -4):
         assert lib.mla_strerror(code)
