@@ -335,6 +335,64 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     assert M.mla_get_error() == 0
 
+    # The widened rows of the path, each timed the same way (graph replay, L2
+    # flushed before each replay, median): gather-and-upconvert on the sweep
+    # cache, the paged decode on the prefill-shaped config, the decode over
+    # 528-byte NoPE rows on the NoPE config.
+    def time_graph(fn, reps=20):
+        fn()
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr):
+            fn()
+        ts = []
+        for it in range(reps + 3):
+            flush.zero_()
+            a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a0.record()
+            gr.replay()
+            a1.record()
+            a1.synchronize()
+            if it >= 3:
+                ts.append(a0.elapsed_time(a1) * 1e-3)
+        ts.sort()
+        return ts[len(ts) // 2]
+
+    widened = {}
+    peak_hbm = load_peaks()[0]
+    if args.workload == "sweep":
+        n_up = 262144
+        up_slots = torch.randint(1, wl.num_slots, (n_up,), generator=torch.Generator().manual_seed(7),
+                                 dtype=torch.int32).to(dev)
+        up_out = torch.empty((n_up, 576), dtype=torch.bfloat16, device=dev)
+        t_up = time_graph(lambda: M.mla_gather_upconvert(cache, up_slots, 64, out=up_out))
+        up_alg = n_up * (4 + 656 + 576 * 2)
+        widened["gather_upconvert"] = {"rows": n_up, "us": t_up * 1e6, "rows_per_s": n_up / t_up,
+                                       "algorithmic_bytes": up_alg, "algorithmic_gbs": up_alg / t_up / 1e9,
+                                       "hbm_frac": up_alg / t_up / 1e9 / peak_hbm}
+        del up_out
+    if args.workload == "prefill" and wl.topk_logical is not None:
+        pos_d = wl.topk_logical.to(dev)
+        bt_d = wl.block_table.to(torch.int32).to(dev)
+        t_phys = time_graph(lambda: M.mla_sparse_decode(q_d, cache, topk_d, db.sm_scale, out=out_d, lse=lse_d,
+                                                        workspace=ws))
+        t_paged = time_graph(lambda: M.mla_sparse_decode_paged(q_d, cache, pos_d, bt_d, wl.page_size, db.sm_scale,
+                                                               out=out_d, lse=lse_d, workspace=ws))
+        widened["paged_decode"] = {"us": t_paged * 1e6, "physical_slots_us": t_phys * 1e6,
+                                   "query_tokens_per_s": db.T / t_paged}
+    if args.workload == "nope":
+        c528 = torch.full((wl.num_slots, 528), wl.slot0_byte, dtype=torch.uint8, device=dev)
+        f = wl.fill
+        M.mla_kv_write(c528, f.slot_idx.to(dev), f.latent.to(dev), None)
+        t656 = time_graph(lambda: M.mla_sparse_decode(q_d, cache, topk_d, db.sm_scale, out=out_d, lse=lse_d,
+                                                      workspace=ws))
+        t528 = time_graph(lambda: M.mla_sparse_decode(q_d, c528, topk_d, db.sm_scale, out=out_d, lse=lse_d,
+                                                      workspace=ws))
+        widened["rows_528"] = {"decode_us": t528 * 1e6, "decode_656_us": t656 * 1e6,
+                               "cache_bytes": int(c528.numel()), "cache_656_bytes": int(cache.numel())}
+        del c528
+    torch.cuda.synchronize()
+    assert M.mla_get_error() == 0
+
     # End to end through the public API with pinned host buffers: per step the
     # inputs go host -> device, the outputs come back device -> host.
     w_in = [] if wb is None else [t for t in (wb.slot_idx, wb.latent, wb.rope) if t is not None]
@@ -416,6 +474,7 @@ def run_ours(args, rank, world, local_rank):
                 "nsplit_workspace_bytes": 0 if ws is None else int(ws.numel()),
             },
             "writer_sweep_us": sweep or None,
+            "widened": widened or None,
             "writer_large": None if fill_pt is None else dict(
                 fill_pt, hbm_frac=fill_pt["algorithmic_gbs"] / peak,
                 note="one call over every slot 1..N-1 (sequential slots), CUDA-graph replay, L2 flushed"),
