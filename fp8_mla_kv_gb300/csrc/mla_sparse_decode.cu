@@ -8,12 +8,14 @@
 // shared memory, so -1, slot 0 and out-of-range indices are never dereferenced.
 //
 // Work decomposition: one CTA per (token, split of the top-k list, group of 16
-// heads); 4 consumer warps and 1 producer warp. Every thread loads a contiguous
+// heads); 4 consumer warps and 2 producer warps. Every thread loads a contiguous
 // run of the split's positions at once (the q loads are issued before them) and
 // one block-wide scan places the present ones in a shared-memory list. The
-// producer copies each listed row global -> shared with one cp.async.bulk (656 B,
+// producers copy each listed row global -> shared with one cp.async.bulk (656 B,
 // or 528 B for NoPE: the tail is not read) into a 4-stage ring of 32-row blocks,
-// each stage completing on an mbarrier.
+// each stage completing on an mbarrier; producer p issues blocks p, p+2, ...
+// (one warp's copy issue is what limits a CTA's row rate, so two issue in
+// parallel).
 //
 // Arithmetic per 32-row block, on tensor cores (m16n8k16, heads as M):
 //   QK  : warp w takes latent tile w (dims 128w .. 128w+127) and RoPE dims
@@ -44,8 +46,9 @@ using namespace mla;
 
 constexpr int kHeads = 16;                   // heads per CTA (M of m16n8k16)
 constexpr int kWarps = 4;                    // consumer warps (one per latent tile)
-constexpr int kProducer = kWarps;            // warp index of the copy-issuing warp
-constexpr int kThreads = (kWarps + 1) * 32;
+constexpr int kProducer = kWarps;            // warp index of the first copy-issuing warp
+constexpr int kProducers = 2;                // copy-issuing warps (alternate blocks)
+constexpr int kThreads = (kWarps + kProducers) * 32;
 constexpr int kConsumerThreads = kWarps * 32;
 constexpr int kNB = 32;                      // rows per block
 constexpr int kStages = 4;
@@ -119,7 +122,7 @@ mla_sparse_decode_kernel(const DecodeArgs args) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], kWarps);
         }
-        *issued_s = 0;
+        issued_s[0] = issued_s[1] = 0;
         fence_mbar_init();
     }
 
@@ -215,10 +218,12 @@ mla_sparse_decode_kernel(const DecodeArgs args) {
     __syncthreads();
     const int nblk = (n_valid + kNB - 1) / kNB;
 
-    if (warp == kProducer) {
-        // ---- producer: lane j copies row j of each block into the stage ring ----
-        int b = 0;
-        for (; b < nblk; ++b) {
+    if (warp >= kProducer) {
+        // ---- producers: warp kProducer + p issues blocks p, p + kProducers, ...;
+        // lane j copies row j of the block into the stage ring ----
+        const int pw = warp - kProducer;
+        int b = pw, cnt = 0;
+        for (; b < nblk; b += kProducers, ++cnt) {
             const int s = b % kStages;
             if (b >= kStages && !mbar_wait_bounded(&empty[s], static_cast<uint32_t>(((b / kStages) - 1) & 1))) {
                 if (lane == 0) atomicOr(args.err, MLA_ERR_PIPELINE_TIMEOUT);
@@ -242,7 +247,7 @@ mla_sparse_decode_kernel(const DecodeArgs args) {
                 bulk_g2s(dst + lane * kRowBytes,
                          args.cache + static_cast<int64_t>(list[b * kNB + lane]) * args.row_bytes, kRowRead, &full[s]);
         }
-        if (lane == 0) *issued_s = b;
+        if (lane == 0) issued_s[pw] = cnt;
         __syncthreads();     // matches the consumers' final barrier
         return;
     }
@@ -479,15 +484,19 @@ mla_sparse_decode_kernel(const DecodeArgs args) {
         if (lane == 0) mbar_arrive(&empty[s]);
     }
 
-    __syncthreads();     // all 5 warps: producer done issuing, consumers done reading
-    if (failed || *issued_s < nblk) {
+    __syncthreads();     // all warps: producers done issuing, consumers done reading
+    if (failed || issued_s[0] + issued_s[1] < nblk) {
         // A wait ran out: record it, let the copies already issued land (bounded)
         // and leave without touching the outputs.
         if (threadIdx.x == 0) {
             atomicOr(args.err, MLA_ERR_PIPELINE_TIMEOUT);
-            const int issued = *issued_s;
-            for (int bb = max(0, issued - kStages); bb < issued; ++bb)
-                (void)mbar_wait_bounded(&full[bb % kStages], static_cast<uint32_t>((bb / kStages) & 1));
+            for (int p = 0; p < kProducers; ++p) {
+                const int cnt = issued_s[p];
+                for (int k = max(0, cnt - kStages / kProducers); k < cnt; ++k) {
+                    const int bb = p + kProducers * k;
+                    (void)mbar_wait_bounded(&full[bb % kStages], static_cast<uint32_t>((bb / kStages) & 1));
+                }
+            }
         }
         return;
     }
