@@ -9,17 +9,18 @@
 // go. Products below 2^-100 are formed in double and rounded once. A NaN code
 // gives 0x7FC0.
 //
-// One warp per row: lane l converts latent values 16l .. 16l+15 (one 16-byte
-// load, two 16-byte stores); lanes 0..7 copy the 128-byte tail (pe_dim 64) or
-// write zeros (pe_dim 0: the tail is not read). An absent slot (<= 0) gives a
-// row of zeros; a slot >= num_slots also sets MLA_ERR_GATHER_INDEX_RANGE.
+// Rows move global -> shared by one cp.async.bulk each (a producer warp, a
+// 4-stage ring of 32-row blocks on mbarriers), then four converter warps widen
+// them: per row, lane l converts latent values 16l .. 16l+15 (two 16-byte
+// stores) and lanes 0..7 store the 128-byte tail (pe_dim 64) or zeros (pe_dim 0:
+// the tail is not read). An absent slot (<= 0) gives a row of zeros; a slot >=
+// num_slots also sets MLA_ERR_GATHER_INDEX_RANGE.
 #include "mla_device.cuh"
 
 namespace {
 
 using namespace mla;
 
-constexpr int kThreads = 256;   // 8 rows in flight per CTA
 constexpr int kOutWidth = kLatent + kRope;   // 576
 
 __device__ __forceinline__ uint32_t product_to_bf16(float v, float s) {
@@ -48,44 +49,143 @@ __device__ __forceinline__ uint32_t product_to_bf16(float v, float s) {
     return hi;
 }
 
-__global__ void __launch_bounds__(kThreads)
+constexpr int kUStages = 4;
+constexpr int kUNB = 32;                              // rows per block
+constexpr int kUWarps = 12;                           // converter warps (rows w, w + 12, w + 24 of a block)
+constexpr int kUProducers = 2;                        // copy-issuing warps (alternate blocks)
+constexpr int kUThreads = (kUWarps + kUProducers) * 32;
+constexpr int kUStageBytes = kUNB * kRowBytes;
+constexpr int kUSmem = kUStages * kUStageBytes + kUStages * kUNB * 4 + 2 * kUStages * 8;
+constexpr int kUCtasPerSm = 2;
+
+// Persistent: CTA c takes blocks c, c + grid, ... of 32 consecutive output rows.
+// The last two warps (producers, alternate blocks) copy each present row global
+// -> shared with one cp.async.bulk into a 4-stage ring and record the block's
+// slots; converter
+// warp w widens rows w, w + 12, w + 24 of the block from shared memory.
+// Two products rounded to BF16 by the hardware conversion (round to nearest even
+// of the fp32 product). That is the nearest BF16 of the exact product unless the
+// fp32 product sits on a BF16 midpoint, is NaN, or is nonzero below 2^-100; such
+// values raise `exact` and are redone by product_to_bf16.
+__device__ __forceinline__ uint32_t pair_to_bf16x2(float v0, float v1, float s, bool& exact) {
+    const float p0 = __fmul_rn(v0, s), p1 = __fmul_rn(v1, s);
+    const uint32_t u0 = __float_as_uint(p0), u1 = __float_as_uint(p1);
+    exact |= ((u0 & 0xFFFFu) == 0x8000u) | ((u1 & 0xFFFFu) == 0x8000u) |
+             ((p0 != 0.0f) & !(fabsf(p0) >= 0x1p-100f)) | ((p1 != 0.0f) & !(fabsf(p1) >= 0x1p-100f));
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(p1), "f"(p0));   // high half <- p1
+    return r;
+}
+
+__global__ void __launch_bounds__(kUThreads, kUCtasPerSm)
 mla_gather_upconvert_kernel(const uint8_t* __restrict__ cache, int64_t num_slots, int64_t row_bytes,
                             const int32_t* __restrict__ slots, int64_t n, int pe_dim,
                             uint16_t* __restrict__ out, int* __restrict__ err) {
-    const int lane = threadIdx.x & 31;
-    const int64_t stride = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
-    for (int64_t r = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; r < n; r += stride) {
-        const int64_t slot = __ldg(slots + r);
-        uint16_t* orow = out + r * kOutWidth;
-        if (slot <= 0 || slot >= num_slots) {
-            if (slot >= num_slots && lane == 0) atomicOr(err, MLA_ERR_GATHER_INDEX_RANGE);
-            const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-            st_v4(orow + 16 * lane, z);
-            st_v4(orow + 16 * lane + 8, z);
-            if (lane < 8) st_v4(orow + kLatent + 8 * lane, z);
-            continue;
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint8_t* stages = smem;
+    int* slot_s = reinterpret_cast<int*>(smem + kUStages * kUStageBytes);      // [stage][row]
+    uint64_t* full = reinterpret_cast<uint64_t*>(slot_s + kUStages * kUNB);
+    uint64_t* empty = full + kUStages;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t nblk = (n + kUNB - 1) / kUNB;
+    const uint32_t row_read = (pe_dim == kRope) ? kRowBytes : kNopeReadBytes;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kUStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kUWarps);
         }
-        const uint8_t* row = cache + slot * row_bytes;
-        const uint4 codes = ld_nc_v4(row + 16 * lane);
-        const float s = __uint_as_float(__ldg(reinterpret_cast<const uint32_t*>(row + kScaleOff) + (lane >> 3)));
-        uint4 tail = make_uint4(0u, 0u, 0u, 0u);
-        if (pe_dim == kRope && lane < 8) tail = ld_nc_v4(row + kTailOff + 16 * lane);
-        const uint32_t w[4] = {codes.x, codes.y, codes.z, codes.w};
-        uint32_t o[8];
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    if (warp >= kUWarps) {
+        // ---- producers: warp kUWarps + p issues the CTA's blocks p, p + 2, ... ----
+        const int pw = warp - kUWarps;
+        const int64_t step = static_cast<int64_t>(kUProducers) * gridDim.x;
+        int64_t blk = blockIdx.x + static_cast<int64_t>(pw) * gridDim.x;
+        int64_t r = blk * kUNB + lane;
+        int next_slot = (blk < nblk && r < n) ? __ldg(slots + r) : 0;
+        for (int k = pw; blk < nblk; k += kUProducers, blk += step) {
+            const int slot = next_slot;
+            const int64_t rn = (blk + step) * kUNB + lane;            // this warp's next block, early
+            next_slot = (blk + step < nblk && rn < n) ? __ldg(slots + rn) : 0;
+            const int s = k % kUStages;
+            if (k >= kUStages && !mbar_wait_bounded(&empty[s], static_cast<uint32_t>(((k / kUStages) - 1) & 1))) {
+                // Record it, let the copies already issued land (bounded), and
+                // leave; the converters' own waits run out on the next block.
+                if (lane == 0) {
+                    atomicOr(err, MLA_ERR_PIPELINE_TIMEOUT);
+                    for (int kk = k - kUStages; kk < k; kk += kUProducers)
+                        (void)mbar_wait_bounded(&full[kk % kUStages], static_cast<uint32_t>((kk / kUStages) & 1));
+                }
+                return;
+            }
+            const bool in_range = blk * kUNB + lane < n;
+            const bool present = in_range && slot > 0 && slot < num_slots;
+            if (in_range && slot >= num_slots) atomicOr(err, MLA_ERR_GATHER_INDEX_RANGE);
+            slot_s[s * kUNB + lane] = present ? slot : (in_range ? 0 : -1);   // -1: past the end
+            const unsigned m = __ballot_sync(0xffffffffu, present);
+            __syncwarp();
+            if (lane == 0) mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(__popc(m)) * row_read);
+            __syncwarp();
+            if (present)
+                bulk_g2s(stages + s * kUStageBytes + lane * kRowBytes, cache + static_cast<int64_t>(slot) * row_bytes,
+                         row_read, &full[s]);
+        }
+        return;
+    }
+
+    // ---- converters ----
+    int64_t blk = blockIdx.x;
+    for (int k = 0; blk < nblk; ++k, blk += gridDim.x) {
+        const int s = k % kUStages;
+        if (!mbar_wait_bounded(&full[s], static_cast<uint32_t>((k / kUStages) & 1))) {
+            if (lane == 0) atomicOr(err, MLA_ERR_PIPELINE_TIMEOUT);
+            return;
+        }
+        const uint8_t* st = stages + s * kUStageBytes;
+        for (int rr = warp; rr < kUNB; rr += kUWarps) {
+            const int slot = slot_s[s * kUNB + rr];
+            if (slot < 0) break;                                      // past the end of the output
+            uint16_t* orow = out + (blk * kUNB + rr) * kOutWidth;
+            if (slot == 0) {                                          // absent: a row of zeros
+                const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+                st_v4(orow + 16 * lane, z);
+                st_v4(orow + 16 * lane + 8, z);
+                if (lane < 8) st_v4(orow + kLatent + 8 * lane, z);
+                continue;
+            }
+            const uint8_t* row = st + rr * kRowBytes;
+            const uint4 codes = *reinterpret_cast<const uint4*>(row + 16 * lane);
+            const float sc = *reinterpret_cast<const float*>(row + kScaleOff + 4 * (lane >> 3));
+            uint4 tail = make_uint4(0u, 0u, 0u, 0u);
+            if (pe_dim == kRope && lane < 8) tail = *reinterpret_cast<const uint4*>(row + kTailOff + 16 * lane);
+            const uint32_t w[4] = {codes.x, codes.y, codes.z, codes.w};
+            float v[16];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            uint32_t h01, h23;
-            e4m3x4_to_f16x2x2(w[i], h01, h23);  // exact
-            const float v0 = __half2float(__ushort_as_half(static_cast<unsigned short>(h01 & 0xFFFFu)));
-            const float v1 = __half2float(__ushort_as_half(static_cast<unsigned short>(h01 >> 16)));
-            const float v2 = __half2float(__ushort_as_half(static_cast<unsigned short>(h23 & 0xFFFFu)));
-            const float v3 = __half2float(__ushort_as_half(static_cast<unsigned short>(h23 >> 16)));
-            o[2 * i] = product_to_bf16(v0, s) | (product_to_bf16(v1, s) << 16);
-            o[2 * i + 1] = product_to_bf16(v2, s) | (product_to_bf16(v3, s) << 16);
+            for (int q = 0; q < 4; ++q) {
+                uint32_t h01, h23;
+                e4m3x4_to_f16x2x2(w[q], h01, h23);  // exact
+                v[4 * q + 0] = __half2float(__ushort_as_half(static_cast<unsigned short>(h01 & 0xFFFFu)));
+                v[4 * q + 1] = __half2float(__ushort_as_half(static_cast<unsigned short>(h01 >> 16)));
+                v[4 * q + 2] = __half2float(__ushort_as_half(static_cast<unsigned short>(h23 & 0xFFFFu)));
+                v[4 * q + 3] = __half2float(__ushort_as_half(static_cast<unsigned short>(h23 >> 16)));
+            }
+            uint32_t o[8];
+            bool exact = false;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) o[q] = pair_to_bf16x2(v[2 * q], v[2 * q + 1], sc, exact);
+            if (exact) {                                              // rare
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    o[q] = product_to_bf16(v[2 * q], sc) | (product_to_bf16(v[2 * q + 1], sc) << 16);
+            }
+            st_v4(orow + 16 * lane, make_uint4(o[0], o[1], o[2], o[3]));
+            st_v4(orow + 16 * lane + 8, make_uint4(o[4], o[5], o[6], o[7]));
+            if (lane < 8) st_v4(orow + kLatent + 8 * lane, tail);
         }
-        st_v4(orow + 16 * lane, make_uint4(o[0], o[1], o[2], o[3]));
-        st_v4(orow + 16 * lane + 8, make_uint4(o[4], o[5], o[6], o[7]));
-        if (lane < 8) st_v4(orow + kLatent + 8 * lane, tail);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
     }
 }
 
@@ -103,11 +203,19 @@ extern "C" int mla_gather_upconvert(mla_kv_cache_t kv, const int32_t* slots, int
     int* err = mla_host::device_error_word();
     const int sms = mla_host::sm_count();
     if (err == nullptr || sms <= 0) return MLA_ECUDA;
-    const int64_t rows_per_cta = kThreads / 32;
-    int64_t blocks = (n + rows_per_cta - 1) / rows_per_cta;
-    const int64_t max_blocks = static_cast<int64_t>(sms) * 8;
-    if (blocks > max_blocks) blocks = max_blocks;
-    mla_gather_upconvert_kernel<<<static_cast<unsigned>(blocks), kThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+    static bool attr_set[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MLA_ECUDA;
+    if (!attr_set[dev]) {
+        if (cudaFuncSetAttribute(mla_gather_upconvert_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kUSmem) !=
+            cudaSuccess)
+            return MLA_ECUDA;
+        attr_set[dev] = true;
+    }
+    const int64_t nblk = (n + kUNB - 1) / kUNB;
+    int64_t grid = static_cast<int64_t>(sms) * kUCtasPerSm;
+    if (grid > nblk) grid = nblk;
+    mla_gather_upconvert_kernel<<<static_cast<unsigned>(grid), kUThreads, kUSmem, static_cast<cudaStream_t>(stream)>>>(
         static_cast<const uint8_t*>(kv.data), kv.num_slots, kv.row_bytes, slots, n, pe_dim,
         static_cast<uint16_t*>(out_bf16), err);
     return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ECUDA;
