@@ -150,3 +150,35 @@ def test_workspace_errors():
     with pytest.raises(M.MlaError) as ei:
         M.mla_sparse_decode(db.q.to(d), g, db.topk.to(d), db.sm_scale, workspace=small)
     assert ei.value.code == M.MLA_ENOWORKSPACE
+
+
+def test_maximum_head_count():
+    # H = 128: eight head groups of 16 in one launch (the largest H the ABI takes).
+    wl = workloads.tiny(H=128, T=2)
+    g, c = build_both(wl)
+    out, lse = gpu_decode(g, wl.decode)
+    check_decode(out, lse, *_ref(c, wl.decode))
+    assert M.mla_get_error() == 0
+
+
+def test_wide_list_split_past_one_cta():
+    # W = 5,000 positions (4,000 present) per token: more than one CTA's list, so
+    # the list is split and the partials merged.
+    wl = workloads.tiny(T=2, W=5000, n_valid=4000, n_rows=4200, num_slots=8192)
+    g, c = build_both(wl)
+    assert M.mla_sparse_decode_workspace_bytes(2, 16, 5000) > 0
+    out, lse = gpu_decode(g, wl.decode)
+    check_decode(out, lse, *_ref(c, wl.decode))
+    assert M.mla_get_error() == 0
+
+
+def test_many_tokens():
+    # T = 2,048 query tokens in one launch, compared on a sample of them.
+    wl = workloads.tiny(T=2048)
+    g, c = build_both(wl)
+    db = wl.decode
+    out, lse = gpu_decode(g, db)
+    tokens = sorted(set(np.random.default_rng(8).choice(db.T, 48, replace=False).tolist()) | {0, db.T - 1})
+    ro, rl, _ = oracle.sparse_decode(db.q, c, db.topk.numpy(), db.sm_scale, tokens=tokens)
+    check_decode(out, lse, ro, rl, tokens=tokens)
+    assert M.mla_get_error() == 0
