@@ -109,9 +109,12 @@ mla_sparse_decode_kernel(const DecodeArgs args) {
     uint64_t* empty = full + kStages;
     int* issued_s = reinterpret_cast<int*>(empty + kStages);
 
-    const int t = blockIdx.x;
+    // blockIdx.x = t * head_groups + hg: the head groups of a token run side by
+    // side and gather the same rows, so all but the first read them from L2.
+    const int head_groups = (args.H + kHeads - 1) / kHeads;
+    const int t = static_cast<int>(blockIdx.x / head_groups);
+    const int hg = static_cast<int>(blockIdx.x % head_groups);
     const int split = blockIdx.y;
-    const int hg = blockIdx.z;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int H = args.H;
@@ -691,7 +694,7 @@ int launch_decode(const void* q_bf16, int T, int H, int d_qk, mla_kv_cache_t kv,
     a.T = T; a.H = H; a.d_qk = d_qk; a.W = W; a.nsplit = nsplit;
     a.split_len = (W + nsplit - 1) / nsplit;
     a.sm_scale_log2 = sm_scale * kLog2e;
-    const dim3 grid(static_cast<unsigned>(T), static_cast<unsigned>(nsplit), static_cast<unsigned>((H + kHeads - 1) / kHeads));
+    const dim3 grid(static_cast<unsigned>(static_cast<int64_t>(T) * ((H + kHeads - 1) / kHeads)), static_cast<unsigned>(nsplit));
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (d_qk == kLatent + kRope)
         mla_sparse_decode_kernel<true><<<grid, kThreads, kSmemTotal, st>>>(a);
