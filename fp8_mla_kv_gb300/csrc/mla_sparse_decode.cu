@@ -8,9 +8,13 @@
 // shared memory, so -1, slot 0 and out-of-range indices are never dereferenced.
 //
 // Work decomposition: one CTA per (token, split of the top-k list, group of 16
-// heads); 4 consumer warps and 2 producer warps. Every thread loads a contiguous
-// run of the split's positions at once (the q loads are issued before them) and
-// one block-wide scan places the present ones in a shared-memory list. The
+// heads), the head groups of a token adjacent in launch order; 4 consumer warps
+// and 2 producer warps. Every thread loads a contiguous run of the split's
+// positions at once (the q loads are issued before them), maps them through the
+// block table when the list holds sequence positions (the paged entry point,
+// vLLM PR #55277 "Relation to #53969"), and one block-wide scan places the
+// present slots in a shared-memory list. Rows are 656 bytes, or 528 for a cache
+// of NoPE rows without a tail (sglang PR #39288, "Relation to other changes"). The
 // producers copy each listed row global -> shared with one cp.async.bulk (656 B,
 // or 528 B for NoPE: the tail is not read) into a 4-stage ring of 32-row blocks,
 // each stage completing on an mbarrier; producer p issues blocks p, p+2, ...
