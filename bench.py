@@ -154,9 +154,19 @@ def oracle_cpu_baseline(wl, cache_np, wb, seconds: float = 12.0):
     t0 = time.perf_counter()
     oracle.sparse_decode(db.q, cache_np, topk, db.sm_scale, tokens=toks, n_threads=cores)
     dt = time.perf_counter() - t0
-    return {"value": n_tok / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": f"float64 oracle decode of {n_tok} of the {db.T} query tokens "
-                      f"(H={db.H}, W={db.W}, all present) in {dt:.2f} s on {cores} threads"}
+    res = {"value": n_tok / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
+           "sample": f"float64 oracle decode of {n_tok} of the {db.T} query tokens "
+                     f"(H={db.H}, W={db.W}, all present) in {dt:.2f} s on {cores} threads",
+           "single_thread": {"value": 1.0 / one, "unit": UNIT, "cores": 1,
+                             "sample": "one query token on one thread"}}
+    if wb is not None:
+        # The oracle writer (one thread) re-writing the step's batch: the same bytes land again.
+        t0 = time.perf_counter()
+        oracle.kv_write(cache_np, wb.slot_idx.numpy(), wb.latent, wb.rope)
+        dtw = time.perf_counter() - t0
+        res["writer_single_thread"] = {"value": int(wb.slot_idx.numel()) / dtw, "unit": "rows/s", "cores": 1,
+                                       "sample": f"the {int(wb.slot_idx.numel())}-row step batch"}
+    return res
 
 
 WORKLOADS = {
