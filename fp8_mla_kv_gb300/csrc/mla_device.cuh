@@ -128,6 +128,16 @@ __device__ __forceinline__ bool bar_sync_or(int id, int nthreads, bool pred) {
     return r != 0;
 }
 
+// Programmatic dependent launch: a kernel may let the next kernel on its stream
+// start launching early; that kernel waits for this one's completion (and its
+// memory) before reading anything. Both are no-ops without the launch attribute.
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // 2^x on the special-function unit (inputs far below the fp32 range give 0).
 __device__ __forceinline__ float ex2_approx(float x) {
     float y;

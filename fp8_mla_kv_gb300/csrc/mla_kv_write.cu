@@ -37,6 +37,9 @@ mla_kv_write_kernel(uint8_t* __restrict__ cache, int64_t num_slots, int64_t row_
                     const uint16_t* __restrict__ latent,
                     const uint16_t* __restrict__ rope,
                     int64_t n_rows, int64_t reserved_slot, int* __restrict__ err) {
+    // A decode launched after this writer may start its set-up now; it waits for
+    // this grid to finish before it reads anything.
+    pdl_launch_dependents();
     const int lane = threadIdx.x & 31;
     const int64_t stride = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
     for (int64_t r = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; r < n_rows;

@@ -124,6 +124,9 @@ mla_sparse_decode_kernel(const DecodeArgs args) {
     const int H = args.H;
     constexpr uint32_t kRowRead = kRopeOn ? kRowBytes : kNopeReadBytes;
 
+    // Launched with programmatic stream serialization: wait for the previous
+    // kernel on the stream (and its memory) before reading any input.
+    pdl_wait();
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&full[s], 1);
@@ -700,11 +703,19 @@ int launch_decode(const void* q_bf16, int T, int H, int d_qk, mla_kv_cache_t kv,
     a.sm_scale_log2 = sm_scale * kLog2e;
     const dim3 grid(static_cast<unsigned>(static_cast<int64_t>(T) * ((H + kHeads - 1) / kHeads)), static_cast<unsigned>(nsplit));
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (d_qk == kLatent + kRope)
-        mla_sparse_decode_kernel<true><<<grid, kThreads, kSmemTotal, st>>>(a);
-    else
-        mla_sparse_decode_kernel<false><<<grid, kThreads, kSmemTotal, st>>>(a);
-    if (cudaGetLastError() != cudaSuccess) return MLA_ECUDA;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemTotal;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t lr = (d_qk == kLatent + kRope) ? cudaLaunchKernelEx(&cfg, mla_sparse_decode_kernel<true>, a)
+                                                     : cudaLaunchKernelEx(&cfg, mla_sparse_decode_kernel<false>, a);
+    if (lr != cudaSuccess || cudaGetLastError() != cudaSuccess) return MLA_ECUDA;
     if (nsplit > 1) {
         mla_split_combine_kernel<<<static_cast<unsigned>(static_cast<int64_t>(T) * H), 128, 0, st>>>(
             a.ws_o, a.ws_lse, H, nsplit, a.out, a.lse);
