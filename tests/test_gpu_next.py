@@ -180,3 +180,32 @@ def test_upconvert_full_size():
     assert bad == 0
     np.testing.assert_array_equal(_bits(out), ref)
     assert M.mla_get_error() == 0
+
+
+def test_paged_with_head_groups_and_splits_equals_physical():
+    """H = 64 (four head groups) and T = 3 (the list is split): an identity block
+    table gives exactly the physical-slot decode."""
+    wl = workloads.small("rope")
+    g, _ = build_both(wl)
+    db = wl.decode
+    d = dev()
+    page = 16
+    bt = torch.arange(wl.num_slots // page, dtype=torch.int32, device=d)
+    ref_out, ref_lse = gpu_decode(g, db)
+    out, lse = M.mla_sparse_decode_paged(db.q.to(d), g, db.topk.to(d), bt, page, db.sm_scale)
+    torch.cuda.synchronize()
+    assert M.mla_sparse_decode_workspace_bytes(db.T, db.H, db.W) > 0
+    assert torch.equal(out.view(torch.int16), ref_out.view(torch.int16)) and torch.equal(lse, ref_lse)
+    assert M.mla_get_error() == 0
+
+
+@pytest.mark.parametrize("n", [0, 1, 31, 33, 95])
+def test_upconvert_partial_blocks(n):
+    wl = workloads.small("sweep")
+    g, c = build_both(wl)
+    slots = np.random.default_rng(n).integers(-1, wl.num_slots, size=n).astype(np.int32)
+    out = M.mla_gather_upconvert(g, torch.from_numpy(slots).to(dev()), 64)
+    torch.cuda.synchronize()
+    ref, _ = oracle.gather_upconvert(c, slots, 64)
+    np.testing.assert_array_equal(_bits(out).reshape(n, 576), ref)
+    assert M.mla_get_error() == 0
