@@ -106,6 +106,11 @@ typedef struct {
  *   reserved_slot the slot writes must never land in (0 in every caller)
  * Precondition: no two rows of one call name the same non-reserved slot (which
  * of them would land is unspecified).
+ * Ordering: the writer lets the next kernel on the stream begin launching while
+ * it runs (programmatic dependent launch); only a kernel launched with
+ * programmatic stream serialization can start early, and such a kernel must
+ * wait for its predecessor (griddepcontrol.wait) before reading the cache, as
+ * mla_sparse_decode does. Ordinary launches and copies are ordered as usual.
  * Returns MLA_OK, MLA_EINVAL or MLA_ECUDA.
  */
 int mla_kv_write(mla_kv_cache_t kv, const int64_t* slot_idx, const void* latent_bf16,
@@ -153,6 +158,9 @@ size_t mla_sparse_decode_workspace_bytes(int T, int H, int W);
  *   workspace  device scratch of at least mla_sparse_decode_workspace_bytes(T,H,W)
  *              bytes, 16-byte aligned (may be NULL when that is 0). Its contents
  *              on entry do not matter; it is clobbered.
+ * The decode kernel is launched with programmatic stream serialization and waits
+ * for the previous kernel on the stream, and its memory, before it reads any
+ * input; behind mla_kv_write its launch overlaps the writer's last CTAs.
  * Returns MLA_OK, MLA_EINVAL, MLA_EUNSUPPORTED, MLA_ENOWORKSPACE or MLA_ECUDA.
  */
 int mla_sparse_decode(const void* q_bf16, int T, int H, int d_qk, mla_kv_cache_t kv,
