@@ -1,7 +1,6 @@
 """Full-size workloads, in the launch configuration the bench times: the whole
-cache is compared byte for byte with the oracle's, and decode outputs are
-compared on sampled tokens the oracle computes one by one (all tokens where
-that is cheap)."""
+cache is compared byte for byte with the oracle's, and the decode output of
+every token and head with the oracle's (a few seconds of oracle time each)."""
 import numpy as np
 import pytest
 import torch
@@ -27,20 +26,14 @@ def _run(wl, tokens, slot0_byte=None):
     return g, errs
 
 
-def _sample(T, k, seed=0):
-    rng = np.random.default_rng(seed)
-    pick = set(rng.choice(T, size=min(k, T), replace=False).tolist()) | {0, T - 1}
-    return sorted(pick)
-
-
 def test_tiny_full():
     wl = workloads.tiny()
-    _run(wl, list(range(wl.decode.T)))
+    _run(wl, None)
 
 
 def test_nope_full_and_slot0_poison():
     wl = workloads.nope()
-    g, _ = _run(wl, list(range(wl.decode.T)))
+    g, _ = _run(wl, None)
     db = wl.decode
     a = gpu_decode(g, db)
     g[0].fill_(0xFF)
@@ -51,14 +44,14 @@ def test_nope_full_and_slot0_poison():
 
 def test_rope_full():
     wl = workloads.rope()
-    _run(wl, _sample(wl.decode.T, 8))
+    _run(wl, None)
 
 
 def test_prefill_full():
     wl = workloads.prefill()
-    _run(wl, sorted(set(_sample(wl.decode.T, 12)) | {1, 63, 64, 65, 511}))
+    _run(wl, None)
 
 
 def test_sweep_full():
     wl = workloads.sweep()
-    _run(wl, _sample(wl.decode.T, 12))
+    _run(wl, None)
