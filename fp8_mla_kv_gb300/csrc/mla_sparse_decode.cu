@@ -36,6 +36,9 @@
 //   PV  : warp w owns output dims 128w .. 128w+127; P (f16, from shared memory)
 //         times scale_row / sigma (sigma = running max of tile w's scales) times
 //         the exact f16 E4M3 codes, with 16-byte V loads; O stays in registers.
+//         What does not need P (sigma, O's rescale when it moves, the f16 pairs
+//         scale_row / sigma, the first V rows) is done before the barriers, off
+//         the path from P to the first PV MMA.
 // Splits write a normalised partial (o, lse) to the caller's workspace and a
 // second kernel merges them in split order (deterministic: no float atomics).
 #include <cfloat>
@@ -376,6 +379,28 @@ mla_sparse_decode_kernel(const DecodeArgs args) {
             red[(warp * 4 + nt) * 32 + lane] =
                 make_float4(fmaf(acc[nt][0], sc[nt][0], accr[nt][0]), fmaf(acc[nt][1], sc[nt][1], accr[nt][1]),
                             fmaf(acc[nt][2], sc[nt][0], accr[nt][2]), fmaf(acc[nt][3], sc[nt][1], accr[nt][3]));
+        // The part of PV that does not need P, ahead of the barriers: sigma (the
+        // running max of tile `warp`'s scales, so p * scale / sigma <= 2^8 in f16),
+        // O rescaled when it moves, and the rows' scale / sigma as f16 pairs.
+        float smax = 0.0f;
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt) smax = fmaxf(smax, fmaxf(sc[nt][0], sc[nt][1]));
+        smax = quad_max(smax);                 // all 32 rows: the same in every lane
+        if (smax > sigma) {
+            const float f = sigma / smax;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                o[i][0] *= f; o[i][1] *= f; o[i][2] *= f; o[i][3] *= f;
+            }
+            sigma = smax;
+            inv_sigma = 1.0f / smax;
+        }
+        uint32_t rs[2][2];
+#pragma unroll
+        for (int kb = 0; kb < 2; ++kb) {
+            rs[kb][0] = pack_f16x2(sc[2 * kb][0] * inv_sigma, sc[2 * kb][1] * inv_sigma);
+            rs[kb][1] = pack_f16x2(sc[2 * kb + 1][0] * inv_sigma, sc[2 * kb + 1][1] * inv_sigma);
+        }
         // Barrier 1 also carries a timeout of any warp to all of them.
         if (bar_sync_or(1, kConsumerThreads, !ok)) { failed = true; break; }
 
@@ -406,6 +431,13 @@ mla_sparse_decode_kernel(const DecodeArgs args) {
         p[3] = ex2_approx(sv[3] - m_ref[1]);
         uint2* pw = reinterpret_cast<uint2*>(pbuf) + warp * 32 + lane;
         *pw = make_uint2(pack_f16x2(p[0], p[1]), pack_f16x2(p[2], p[3]));
+        // V rows of the first PV step: loaded before barrier 2 (they do not depend on P).
+        const uint8_t* vb = st + 128 * warp + 16 * g;
+        uint4 Vn[4];
+        Vn[0] = *reinterpret_cast<const uint4*>(vb + (2 * c + 0) * kRowBytes);
+        Vn[1] = *reinterpret_cast<const uint4*>(vb + (2 * c + 1) * kRowBytes);
+        Vn[2] = *reinterpret_cast<const uint4*>(vb + (2 * c + 8) * kRowBytes);
+        Vn[3] = *reinterpret_cast<const uint4*>(vb + (2 * c + 9) * kRowBytes);
         if (bar_sync_or(1, kConsumerThreads, need)) {
             // Rare after the first block: move the offsets of the heads whose
             // block maximum ran ahead, rescale O and l, and rewrite this warp's P.
@@ -437,20 +469,7 @@ mla_sparse_decode_kernel(const DecodeArgs args) {
         l_run[0] += p[0] + p[1];
         l_run[1] += p[2] + p[3];
 
-        // (3) PV of tile `warp`. sigma keeps p * scale / sigma <= 2^8 in f16.
-        float smax = 0.0f;
-#pragma unroll
-        for (int nt = 0; nt < 4; ++nt) smax = fmaxf(smax, fmaxf(sc[nt][0], sc[nt][1]));
-        smax = quad_max(smax);                 // all 32 rows: the same in every lane
-        if (smax > sigma) {
-            const float f = sigma / smax;
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                o[i][0] *= f; o[i][1] *= f; o[i][2] *= f; o[i][3] *= f;
-            }
-            sigma = smax;
-            inv_sigma = 1.0f / smax;
-        }
+        // (3) PV of tile `warp`.
         const uint2* pr = reinterpret_cast<const uint2*>(pbuf) + lane;
 #pragma unroll
         for (int kb = 0; kb < 2; ++kb) {
@@ -458,8 +477,8 @@ mla_sparse_decode_kernel(const DecodeArgs args) {
             // row's tile scale / sigma.
             const uint2 plo = pr[(2 * kb) * 32];
             const uint2 phi = pr[(2 * kb + 1) * 32];
-            const uint32_t r01 = pack_f16x2(sc[2 * kb][0] * inv_sigma, sc[2 * kb][1] * inv_sigma);
-            const uint32_t r89 = pack_f16x2(sc[2 * kb + 1][0] * inv_sigma, sc[2 * kb + 1][1] * inv_sigma);
+            const uint32_t r01 = rs[kb][0];
+            const uint32_t r89 = rs[kb][1];
             uint32_t pa[4];
             pa[0] = hmul2(plo.x, r01);
             pa[1] = hmul2(plo.y, r01);
@@ -468,11 +487,10 @@ mla_sparse_decode_kernel(const DecodeArgs args) {
             // B: V rows j0, j0+1, j0+8, j0+9; lane g takes dims 128w + 16g .. +15,
             // so n-tile (q, i) column n is dim 128w + 16n + 4q + i.
             const int j0 = 16 * kb + 2 * c;
-            const uint8_t* vb = st + 128 * warp + 16 * g;
-            const uint4 V0 = *reinterpret_cast<const uint4*>(vb + (j0 + 0) * kRowBytes);
-            const uint4 V1 = *reinterpret_cast<const uint4*>(vb + (j0 + 1) * kRowBytes);
-            const uint4 V2 = *reinterpret_cast<const uint4*>(vb + (j0 + 8) * kRowBytes);
-            const uint4 V3 = *reinterpret_cast<const uint4*>(vb + (j0 + 9) * kRowBytes);
+            const uint4 V0 = kb == 0 ? Vn[0] : *reinterpret_cast<const uint4*>(vb + (j0 + 0) * kRowBytes);
+            const uint4 V1 = kb == 0 ? Vn[1] : *reinterpret_cast<const uint4*>(vb + (j0 + 1) * kRowBytes);
+            const uint4 V2 = kb == 0 ? Vn[2] : *reinterpret_cast<const uint4*>(vb + (j0 + 8) * kRowBytes);
+            const uint4 V3 = kb == 0 ? Vn[3] : *reinterpret_cast<const uint4*>(vb + (j0 + 9) * kRowBytes);
 #pragma unroll
             for (int qd = 0; qd < 4; ++qd) {
                 const uint32_t W0 = qd == 0 ? V0.x : qd == 1 ? V0.y : qd == 2 ? V0.z : V0.w;
