@@ -9,9 +9,9 @@
 // go. Products below 2^-100 are formed in double and rounded once. A NaN code
 // gives 0x7FC0.
 //
-// Rows move global -> shared by one cp.async.bulk each (a producer warp, a
-// 4-stage ring of 32-row blocks on mbarriers), then four converter warps widen
-// them: per row, lane l converts latent values 16l .. 16l+15 (two 16-byte
+// Rows move global -> shared by one cp.async.bulk each (two producer warps
+// taking alternate blocks, a 5-stage ring of 32-row blocks on mbarriers), then
+// twelve converter warps widen them: per row, lane l converts latent values 16l .. 16l+15 (two 16-byte
 // stores) and lanes 0..7 store the 128-byte tail (pe_dim 64) or zeros (pe_dim 0:
 // the tail is not read). An absent slot (<= 0) gives a row of zeros; a slot >=
 // num_slots also sets MLA_ERR_GATHER_INDEX_RANGE.
@@ -49,7 +49,7 @@ __device__ __forceinline__ uint32_t product_to_bf16(float v, float s) {
     return hi;
 }
 
-constexpr int kUStages = 4;
+constexpr int kUStages = 5;
 constexpr int kUNB = 32;                              // rows per block
 constexpr int kUWarps = 12;                           // converter warps (rows w, w + 12, w + 24 of a block)
 constexpr int kUProducers = 2;                        // copy-issuing warps (alternate blocks)
@@ -60,7 +60,7 @@ constexpr int kUCtasPerSm = 2;
 
 // Persistent: CTA c takes blocks c, c + grid, ... of 32 consecutive output rows.
 // The last two warps (producers, alternate blocks) copy each present row global
-// -> shared with one cp.async.bulk into a 4-stage ring and record the block's
+// -> shared with one cp.async.bulk into a 5-stage ring and record the block's
 // slots; converter
 // warp w widens rows w, w + 12, w + 24 of the block from shared memory.
 // Two products rounded to BF16 by the hardware conversion (round to nearest even
@@ -115,7 +115,7 @@ mla_gather_upconvert_kernel(const uint8_t* __restrict__ cache, int64_t num_slots
                 // leave; the converters' own waits run out on the next block.
                 if (lane == 0) {
                     atomicOr(err, MLA_ERR_PIPELINE_TIMEOUT);
-                    for (int kk = k - kUStages; kk < k; kk += kUProducers)
+                    for (int kk = k - kUProducers; kk >= 0 && kk >= k - kUStages; kk -= kUProducers)
                         (void)mbar_wait_bounded(&full[kk % kUStages], static_cast<uint32_t>((kk / kUStages) & 1));
                 }
                 return;
