@@ -1,0 +1,125 @@
+"""The seeded input generators: the same seed gives the same bits, another seed
+other data, and each workload has the structure its configuration states (slot
+ranges, distinct entries, -1 padding, active lengths, the causal block-table
+layout, padding rows aimed at slot 0). CPU only; the reduced variants."""
+import inspect
+import os
+import sys
+
+import numpy as np
+import pytest
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, os.path.dirname(HERE))
+
+from fp8_mla_kv_gb300 import workloads  # noqa: E402
+
+NAMES = ["tiny", "nope", "rope", "prefill", "sweep"]
+
+
+def _tensors(wl):
+    out = []
+    for wb in ([wl.fill] if wl.fill is not None else []) + list(wl.writes):
+        out += [wb.slot_idx, wb.latent] + ([wb.rope] if wb.rope is not None else [])
+    out += [wl.decode.q, wl.decode.topk]
+    for t in (wl.block_table, wl.topk_logical):
+        if t is not None:
+            out.append(t)
+    return out
+
+
+def _same(a, b):
+    """Same dtype, shape and bytes (so NaN payloads and signed zeros count)."""
+    return (a.dtype == b.dtype and a.shape == b.shape and
+            torch.equal(a.contiguous().view(torch.uint8), b.contiguous().view(torch.uint8)))
+
+
+@pytest.mark.parametrize("name", NAMES)
+def test_same_seed_same_bits_other_seed_other_data(name):
+    a, b = workloads.small(name, seed=0), workloads.small(name, seed=0)
+    ta, tb = _tensors(a), _tensors(b)
+    assert len(ta) == len(tb) and all(_same(x, y) for x, y in zip(ta, tb))
+    c = workloads.small(name, seed=1)
+    assert not torch.equal(a.decode.q.view(torch.int16), c.decode.q.view(torch.int16))
+
+
+def _present_rows_distinct(topk, num_slots):
+    for row in topk.numpy():
+        p = row[row >= 0]
+        assert (p >= 1).all() and (p < num_slots).all()
+        assert len(np.unique(p)) == len(p)
+
+
+def test_tiny_structure():
+    wl = workloads.tiny()
+    wb = wl.writes[0]
+    slots = wb.slot_idx.numpy()
+    real = slots[slots != 0]
+    assert len(real) == 256 and len(np.unique(real)) == 256 and real.min() >= 1 and real.max() < 4096
+    assert (slots == 0).sum() == 32
+    assert torch.isnan(wb.latent[torch.from_numpy(slots == 0)].float()).all()
+    topk = wl.decode.topk.numpy()
+    assert topk.shape == (4, 128)
+    assert (topk[:, :80] > 0).all() and (topk[:, 80:] == -1).all()
+    assert np.isin(topk[:, :80], real).all()
+    _present_rows_distinct(wl.decode.topk, wl.num_slots)
+    assert wl.decode.q.shape == (4, 16, 576) and wl.slot0_byte == 0
+
+
+def test_nope_structure():
+    wl = workloads.small("nope")
+    topk = wl.decode.topk.numpy()
+    lens = (topk >= 0).sum(1)
+    assert (lens >= 1).all() and (lens <= 256).all()
+    for row, n in zip(topk, lens):
+        assert (row[:n] > 0).all() and (row[n:] == -1).all()     # active prefix, -1 tail
+    _present_rows_distinct(wl.decode.topk, wl.num_slots)
+    assert wl.fill.rope is None and wl.decode.d_qk == 512
+    full = inspect.signature(workloads.nope).parameters
+    assert full["W"].default == 2176 and full["max_len"].default == 2048   # a 2,048 list + 128-wide tail
+
+
+def test_rope_structure_and_outliers():
+    wl = workloads.small("rope")
+    assert (wl.decode.topk.numpy() > 0).all()
+    _present_rows_distinct(wl.decode.topk, wl.num_slots)
+    lat = wl.fill.latent.float()
+    # N(0,1) with 1 % of values x20: |x| > 6 is essentially only the outliers
+    frac = (lat.abs() > 6).float().mean().item()
+    assert 0.005 < frac < 0.012
+    assert wl.decode.H == 64 and abs(wl.decode.sm_scale - 192 ** -0.5) < 1e-12
+
+
+def test_prefill_causal_block_table():
+    wl = workloads.small("prefill")
+    page = wl.page_size
+    table = wl.block_table.numpy()
+    assert len(np.unique(table)) == len(table) and table.min() >= 1     # page 0 holds the reserved slot
+    lg = wl.topk_logical.numpy()
+    T, W = lg.shape
+    for i in range(T):
+        k = min(i + 1, W)
+        row = lg[i]
+        assert (row[k:] == -1).all()
+        chosen = row[:k]
+        assert len(np.unique(chosen)) == k and chosen.min() >= 0 and chosen.max() <= i
+    phys = np.where(lg >= 0, table[np.maximum(lg, 0) // page] * page + np.maximum(lg, 0) % page, -1)
+    np.testing.assert_array_equal(phys, wl.decode.topk.numpy())
+    assert wl.slot0_byte == 0xFF
+
+
+def test_sweep_writer_batches():
+    wl = workloads.small("sweep")
+    sizes = [wb.slot_idx.numel() for wb in wl.writes]
+    assert sizes == [1, 1, 64, 64, 1024, 1024]
+    for wb in wl.writes:
+        s = wb.slot_idx.numpy()
+        real = s[s != 0]
+        assert len(np.unique(real)) == len(real) and (real >= 1).all() and (real < wl.num_slots).all()
+        if wb.label.endswith(".valid"):
+            assert (s != 0).all()
+    padded = wl.writes[-1].slot_idx.numpy()
+    assert 0.15 < (padded == 0).mean() < 0.35                            # a random 25 % aimed at slot 0
+    assert (wl.decode.topk.numpy() > 0).all()
+    _present_rows_distinct(wl.decode.topk, wl.num_slots)
