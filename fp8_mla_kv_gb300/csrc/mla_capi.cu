@@ -1,6 +1,8 @@
 // Host-side plumbing of libmlasparse: the device error word, SM-count cache,
 // mla_get_error and mla_strerror.
 #include <mutex>
+#include <utility>
+#include <vector>
 
 #include "mla_device.cuh"
 
@@ -12,6 +14,7 @@ __device__ int g_mla_error_word = 0;
 constexpr int kMaxDevices = 64;
 int* g_err_addr[kMaxDevices] = {};
 int g_sms[kMaxDevices] = {};
+std::vector<std::pair<int, const void*>> g_smem_set;   // (device, kernel) pairs already raised
 std::mutex g_mu;
 
 int current_device() {
@@ -46,6 +49,17 @@ int sm_count() {
         g_sms[dev] = n;
     }
     return g_sms[dev];
+}
+
+bool max_dynamic_smem(const void* kernel, int bytes) {
+    const int dev = current_device();
+    if (dev < 0) return false;
+    std::lock_guard<std::mutex> lk(g_mu);
+    for (const auto& p : g_smem_set)
+        if (p.first == dev && p.second == kernel) return true;
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess) return false;
+    g_smem_set.emplace_back(dev, kernel);
+    return true;
 }
 
 }  // namespace mla_host

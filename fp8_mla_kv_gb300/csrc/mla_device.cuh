@@ -192,4 +192,7 @@ __device__ __forceinline__ float bf16hi(uint32_t v) { return __uint_as_float(v &
 namespace mla_host {
 int* device_error_word();          // device address of this device's error word (nullptr on failure)
 int sm_count();                    // SM count of the current device (0 on failure)
+// Raise a kernel's dynamic shared-memory limit to `bytes` on the current device,
+// once per (device, kernel) under a lock; false if the runtime refuses.
+bool max_dynamic_smem(const void* kernel, int bytes);
 }

@@ -203,15 +203,8 @@ extern "C" int mla_gather_upconvert(mla_kv_cache_t kv, const int32_t* slots, int
     int* err = mla_host::device_error_word();
     const int sms = mla_host::sm_count();
     if (err == nullptr || sms <= 0) return MLA_ECUDA;
-    static bool attr_set[64] = {};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MLA_ECUDA;
-    if (!attr_set[dev]) {
-        if (cudaFuncSetAttribute(mla_gather_upconvert_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kUSmem) !=
-            cudaSuccess)
-            return MLA_ECUDA;
-        attr_set[dev] = true;
-    }
+    if (!mla_host::max_dynamic_smem(reinterpret_cast<const void*>(mla_gather_upconvert_kernel), kUSmem))
+        return MLA_ECUDA;
     const int64_t nblk = (n + kUNB - 1) / kUNB;
     int64_t grid = static_cast<int64_t>(sms) * kUCtasPerSm;
     if (grid > nblk) grid = nblk;
