@@ -169,8 +169,9 @@ int mla_sparse_decode(const void* q_bf16, int T, int H, int d_qk, mla_kv_cache_t
 
 /*
  * mla_sparse_decode_paged - mla_sparse_decode with the top-k list given as
- * sequence positions and a block table (vLLM PR #55277, "Relation to #53969":
- * the indexer emits logical positions that the kernel maps to cache slots).
+ * sequence positions and a block table (vLLM PR #55277, Purpose item 2: the
+ * sparse attention reads its top-k entries through block tables, a page table
+ * whose width is a capacity; here the kernel maps each position to a slot).
  *
  * Entry j of token t is position p = topk_pos[t,j] of the token's sequence
  * s = token_seq[t] (every token uses row 0 when token_seq is NULL). It stands for

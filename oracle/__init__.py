@@ -194,7 +194,7 @@ def sparse_decode(q, cache: np.ndarray, topk, sm_scale: float, tokens=None,
 
 def paged_to_physical(topk_logical, block_table, page_size: int, token_seq=None):
     """Physical slots of a top-k list given as sequence positions (vLLM PR #55277,
-    "Relation to #53969": the indexer's positions go through the block table).
+    Purpose item 2: the sparse top-k entries are read through block tables).
 
     topk_logical: int32 [T, W], -1 (any negative) = absent. block_table: int32
     [n_seq, max_pages], the physical page of each logical page; a negative entry
