@@ -189,6 +189,95 @@ WORKLOADS = {
 }
 
 
+def time_graph(flush, fn, reps=20, calls=1):
+    """Seconds per call of fn: `calls` calls captured in one CUDA graph, the graph
+    replayed `reps` times (after 3 untimed replays) with L2 flushed before each
+    replay, CUDA events around each replay; the median replay divided by calls."""
+    fn()
+    torch.cuda.synchronize()
+    gr = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gr):
+        for _ in range(calls):
+            fn()
+    ts = []
+    for it in range(reps + 3):
+        flush.zero_()
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record()
+        gr.replay()
+        a1.record()
+        a1.synchronize()
+        if it >= 3:
+            ts.append(a0.elapsed_time(a1) * 1e-3 / calls)
+    ts.sort()
+    del gr
+    return ts[len(ts) // 2]
+
+
+def load_bf16_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops"]), "measured"
+    return 1900.0, "fallback"
+
+
+def decode_figures(db, num_slots, t_s, row_read=None):
+    """Throughput, algorithmic bytes and flops of one decode call of db taking t_s."""
+    n_valid = int(((db.topk > 0) & (db.topk < num_slots)).sum())
+    rr = row_read or (656 if db.d_qk == 576 else 528)
+    gathered = n_valid * rr
+    alg = gathered + db.T * db.W * 4 + db.T * db.H * db.d_qk * 2 + db.T * db.H * 512 * 2 + db.T * db.H * 4
+    flops = 2.0 * n_valid * db.H * (db.d_qk + 512)
+    hbm, _ = load_peaks()
+    tf, _ = load_bf16_peak()
+    return {"us": t_s * 1e6, "query_tokens_per_s": db.T / t_s, "present_entries": n_valid,
+            "gathered_bytes": gathered, "gathered_kv_gbs": gathered / t_s / 1e9,
+            "algorithmic_bytes": alg, "algorithmic_gbs": alg / t_s / 1e9, "hbm_frac": alg / t_s / 1e9 / hbm,
+            "tflops": flops / t_s / 1e12, "tensor_frac_of_bf16_peak": flops / t_s / 1e12 / tf}
+
+
+def measure_configs(dev, flush):
+    """The four other configurations: decode timed by graph replay with L2 flushed
+    before each replay (median), plus the 528-byte rows (NoPE) and the paged entry
+    point (prefill)."""
+    from fp8_mla_kv_gb300 import mlasparse as M
+    res = {}
+    for name in ("tiny", "nope", "rope", "prefill"):
+        wl = workloads.by_name(name)
+        cache = build_cache_gpu(wl, dev)
+        for w in wl.writes:
+            M.mla_kv_write(cache, w.slot_idx.to(dev), w.latent.to(dev), None if w.rope is None else w.rope.to(dev))
+        db = wl.decode
+        q, tk = db.q.to(dev), db.topk.to(dev)
+        out = torch.empty((db.T, db.H, 512), dtype=torch.bfloat16, device=dev)
+        lse = torch.empty((db.T, db.H), dtype=torch.float32, device=dev)
+        ws = M.alloc_workspace(db.T, db.H, db.W, dev)
+        t = time_graph(flush, lambda: M.mla_sparse_decode(q, cache, tk, db.sm_scale, out=out, lse=lse, workspace=ws))
+        rec = decode_figures(db, wl.num_slots, t)
+        rec["shape"] = {"T": db.T, "H": db.H, "d_qk": db.d_qk, "W": db.W, "num_slots": wl.num_slots}
+        if name == "nope":
+            c528 = torch.full((wl.num_slots, 528), wl.slot0_byte, dtype=torch.uint8, device=dev)
+            f = wl.fill
+            M.mla_kv_write(c528, f.slot_idx.to(dev), f.latent.to(dev), None)
+            t528 = time_graph(flush, lambda: M.mla_sparse_decode(q, c528, tk, db.sm_scale, out=out, lse=lse,
+                                                                  workspace=ws))
+            rec["rows_528"] = decode_figures(db, wl.num_slots, t528, row_read=528)
+            rec["rows_528"]["cache_bytes"] = int(c528.numel())
+            del c528
+        if name == "prefill":
+            pos, bt = wl.topk_logical.to(dev), wl.block_table.to(torch.int32).to(dev)
+            tp = time_graph(flush, lambda: M.mla_sparse_decode_paged(q, cache, pos, bt, wl.page_size, db.sm_scale,
+                                                                     out=out, lse=lse, workspace=ws))
+            rec["paged"] = decode_figures(db, wl.num_slots, tp)
+        res[name] = rec
+        del cache, q, tk, out, lse, ws
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+    return res
+
+
 def step_write_batch(wl):
     for w in wl.writes:
         if w.label == WRITE_LABEL:
@@ -307,81 +396,52 @@ def run_ours(args, rank, world, local_rank):
     d_ms = [ev2[k][1].elapsed_time(ev2[k][2]) for k in range(K2)]
     assert M.mla_get_error() == 0
 
-    # Writer sweep (every batch of the workload), each call a replayed graph.
+    # Writer sweep (every batch of the workload). Two figures per batch: the pages'
+    # method (sglang PR #47013, Speed Tests: CUDA-graph replay) with 100 calls in
+    # one graph, reported per call (L2 flushed once before each replay, the 100
+    # calls then run back to back), and one call per graph replay with L2 flushed.
     sweep = {}
     for w in wl.writes:
         sd, ld = w.slot_idx.to(dev), w.latent.to(dev)
         rd = None if w.rope is None else w.rope.to(dev)
-        M.mla_kv_write(cache, sd, ld, rd)
-        gw = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(gw):
-            M.mla_kv_write(cache, sd, ld, rd)
-        ts = []
-        for it in range(25):
-            flush.zero_()
-            a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a0.record()
-            gw.replay()
-            a1.record()
-            a1.synchronize()
-            if it >= 5:
-                ts.append(a0.elapsed_time(a1) * 1e3)
-        ts.sort()
-        sweep[w.label] = {"rows": int(w.slot_idx.numel()), "written": int((w.slot_idx > 0).sum()),
-                          "us": ts[len(ts) // 2]}
-    # Large-N writer point: the workload's whole fill (every slot but the reserved
-    # one) in one call, re-writing the same rows so the cache contents stay as they are.
+        t_one = time_graph(flush, lambda: M.mla_kv_write(cache, sd, ld, rd), reps=20)
+        t_100 = time_graph(flush, lambda: M.mla_kv_write(cache, sd, ld, rd), reps=10, calls=100)
+        n_rows, n_wr = int(w.slot_idx.numel()), int((w.slot_idx > 0).sum())
+        alg = n_wr * (1024 + (128 if rd is not None else 0) + 656) + n_rows * 8
+        sweep[w.label] = {"rows": n_rows, "written": n_wr, "us_per_call_graph100": t_100 * 1e6,
+                          "us_single_call": t_one * 1e6, "rows_per_s": n_rows / t_100,
+                          "hbm_frac_graph100": alg / t_100 / 1e9 / load_peaks()[0]}
+    # Large-N writer points over every slot but the reserved one, in one call:
+    # the workload's own fill (sequential slots, re-writing the same rows so the
+    # cache contents stay as they are), and the same rows scattered to a random
+    # permutation of the slots of a second cache of the same size.
     fill_pt = None
     f = wl.fill
     if f is not None and args.workload == "sweep":
         fs, fl = f.slot_idx.to(dev), f.latent.to(dev)
         fr = None if f.rope is None else f.rope.to(dev)
-        M.mla_kv_write(cache, fs, fl, fr)
-        gf = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(gf):
-            M.mla_kv_write(cache, fs, fl, fr)
-        ts = []
-        for it in range(8):
-            flush.zero_()
-            a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a0.record()
-            gf.replay()
-            a1.record()
-            a1.synchronize()
-            if it >= 3:
-                ts.append(a0.elapsed_time(a1) * 1e-3)
-        ts.sort()
-        t_fill = ts[len(ts) // 2]
         n_fill = int(fs.numel())
         fill_alg = n_fill * (1024 + (128 if fr is not None else 0) + 656 + 8)
-        fill_pt = {"rows": n_fill, "us": t_fill * 1e6, "rows_per_s": n_fill / t_fill,
-                   "algorithmic_bytes": fill_alg, "algorithmic_gbs": fill_alg / t_fill / 1e9}
-        del fs, fl, fr, gf
+        t_seq = time_graph(flush, lambda: M.mla_kv_write(cache, fs, fl, fr), reps=5)
+        perm = (torch.randperm(n_fill, generator=torch.Generator().manual_seed(11)) + 1).to(torch.int64).to(dev)
+        cache2 = torch.zeros_like(cache)
+        t_rnd = time_graph(flush, lambda: M.mla_kv_write(cache2, perm, fl, fr), reps=5)
+        peak_hbm = load_peaks()[0]
+        fill_pt = {
+            "sequential": {"rows": n_fill, "us": t_seq * 1e6, "rows_per_s": n_fill / t_seq,
+                           "algorithmic_gbs": fill_alg / t_seq / 1e9, "hbm_frac": fill_alg / t_seq / 1e9 / peak_hbm},
+            "random": {"rows": n_fill, "us": t_rnd * 1e6, "rows_per_s": n_fill / t_rnd,
+                       "algorithmic_gbs": fill_alg / t_rnd / 1e9, "hbm_frac": fill_alg / t_rnd / 1e9 / peak_hbm},
+            "algorithmic_bytes": fill_alg,
+            "note": "one call over every slot 1..N-1 (sequential slots / a random permutation into a second "
+                    "1,048,576-slot cache), CUDA-graph replay, L2 flushed",
+        }
+        del fs, fl, fr, perm, cache2
     torch.cuda.synchronize()
     assert M.mla_get_error() == 0
 
     # The widened rows of the path, each timed the same way (graph replay, L2
-    # flushed before each replay, median): gather-and-upconvert on the sweep
-    # cache, the paged decode on the prefill-shaped config, the decode over
-    # 528-byte NoPE rows on the NoPE config.
-    def time_graph(fn, reps=20):
-        fn()
-        gr = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(gr):
-            fn()
-        ts = []
-        for it in range(reps + 3):
-            flush.zero_()
-            a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a0.record()
-            gr.replay()
-            a1.record()
-            a1.synchronize()
-            if it >= 3:
-                ts.append(a0.elapsed_time(a1) * 1e-3)
-        ts.sort()
-        return ts[len(ts) // 2]
-
+    # flushed before each replay, median): gather-and-upconvert on the sweep cache.
     widened = {}
     peak_hbm = load_peaks()[0]
     if args.workload == "sweep":
@@ -389,32 +449,20 @@ def run_ours(args, rank, world, local_rank):
         up_slots = torch.randint(1, wl.num_slots, (n_up,), generator=torch.Generator().manual_seed(7),
                                  dtype=torch.int32).to(dev)
         up_out = torch.empty((n_up, 576), dtype=torch.bfloat16, device=dev)
-        t_up = time_graph(lambda: M.mla_gather_upconvert(cache, up_slots, 64, out=up_out))
+        t_up = time_graph(flush, lambda: M.mla_gather_upconvert(cache, up_slots, 64, out=up_out))
         up_alg = n_up * (4 + 656 + 576 * 2)
         widened["gather_upconvert"] = {"rows": n_up, "us": t_up * 1e6, "rows_per_s": n_up / t_up,
                                        "algorithmic_bytes": up_alg, "algorithmic_gbs": up_alg / t_up / 1e9,
                                        "hbm_frac": up_alg / t_up / 1e9 / peak_hbm}
         del up_out
-    if args.workload == "prefill" and wl.topk_logical is not None:
-        pos_d = wl.topk_logical.to(dev)
-        bt_d = wl.block_table.to(torch.int32).to(dev)
-        t_phys = time_graph(lambda: M.mla_sparse_decode(q_d, cache, topk_d, db.sm_scale, out=out_d, lse=lse_d,
-                                                        workspace=ws))
-        t_paged = time_graph(lambda: M.mla_sparse_decode_paged(q_d, cache, pos_d, bt_d, wl.page_size, db.sm_scale,
-                                                               out=out_d, lse=lse_d, workspace=ws))
-        widened["paged_decode"] = {"us": t_paged * 1e6, "physical_slots_us": t_phys * 1e6,
-                                   "query_tokens_per_s": db.T / t_paged}
-    if args.workload == "nope":
-        c528 = torch.full((wl.num_slots, 528), wl.slot0_byte, dtype=torch.uint8, device=dev)
-        f = wl.fill
-        M.mla_kv_write(c528, f.slot_idx.to(dev), f.latent.to(dev), None)
-        t656 = time_graph(lambda: M.mla_sparse_decode(q_d, cache, topk_d, db.sm_scale, out=out_d, lse=lse_d,
-                                                      workspace=ws))
-        t528 = time_graph(lambda: M.mla_sparse_decode(q_d, c528, topk_d, db.sm_scale, out=out_d, lse=lse_d,
-                                                      workspace=ws))
-        widened["rows_528"] = {"decode_us": t528 * 1e6, "decode_656_us": t656 * 1e6,
-                               "cache_bytes": int(c528.numel()), "cache_656_bytes": int(cache.numel())}
-        del c528
+    torch.cuda.synchronize()
+    assert M.mla_get_error() == 0
+
+    # The other four configurations, measured in the same run with the same method
+    # (their own caches, decode graph-replayed, L2 flushed before each replay).
+    configs = None
+    if args.workload == "sweep" and not args.no_configs:
+        configs = measure_configs(dev, flush)
     torch.cuda.synchronize()
     assert M.mla_get_error() == 0
 
@@ -539,11 +587,10 @@ def run_ours(args, rank, world, local_rank):
                 "gathered_bytes": gathered,
                 "nsplit_workspace_bytes": 0 if ws is None else int(ws.numel()),
             },
-            "writer_sweep_us": sweep or None,
+            "writer_sweep": sweep or None,
             "widened": widened or None,
-            "writer_large": None if fill_pt is None else dict(
-                fill_pt, hbm_frac=fill_pt["algorithmic_gbs"] / peak,
-                note="one call over every slot 1..N-1 (sequential slots), CUDA-graph replay, L2 flushed"),
+            "writer_large": fill_pt,
+            "configs": configs,
             "writer": None if wb is None else {
                 "us": writer_ms * 1e3,
                 "rows_per_s": job_rate(world, n_rows, writer_ms * 1e-3),
@@ -629,6 +676,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-configs", action="store_true")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="sweep")
     args = ap.parse_args()
     rank, world, local_rank = dist_env()

@@ -31,14 +31,18 @@ __device__ __forceinline__ uint32_t quant2(float x0, float x1, float scale, floa
     return static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(v, __NV_SATFINITE, __NV_E4M3));
 }
 
-__global__ void __launch_bounds__(kWriterThreads)
+__global__ void __launch_bounds__(kWriterThreads, 8)
 mla_kv_write_kernel(uint8_t* __restrict__ cache, int64_t num_slots, int64_t row_bytes,
                     const int64_t* __restrict__ slot_idx,
                     const uint16_t* __restrict__ latent,
                     const uint16_t* __restrict__ rope,
                     int64_t n_rows, int64_t reserved_slot, int* __restrict__ err) {
-    // A decode launched after this writer may start its set-up now; it waits for
-    // this grid to finish before it reads anything.
+    // Launched with programmatic stream serialization: the CTAs may be resident
+    // before the previous kernel on the stream finishes; nothing is read before it
+    // has (with its memory). A kernel launched after this writer the same way (the
+    // decode, or the next writer call) may start its set-up now; it waits for this
+    // grid to finish before it reads anything.
+    pdl_wait();
     pdl_launch_dependents();
     const int lane = threadIdx.x & 31;
     const int64_t stride = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
@@ -116,8 +120,18 @@ extern "C" int mla_kv_write(mla_kv_cache_t kv, const int64_t* slot_idx, const vo
     int64_t blocks = (n_rows + rows_per_cta - 1) / rows_per_cta;
     const int64_t max_blocks = static_cast<int64_t>(sms) * 8;     // 64 resident warps per SM
     if (blocks > max_blocks) blocks = max_blocks;
-    mla_kv_write_kernel<<<static_cast<unsigned>(blocks), kWriterThreads, 0, static_cast<cudaStream_t>(stream)>>>(
-        static_cast<uint8_t*>(kv.data), kv.num_slots, kv.row_bytes, slot_idx, static_cast<const uint16_t*>(latent_bf16),
-        static_cast<const uint16_t*>(rope_bf16), n_rows, reserved_slot, err);
-    return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ECUDA;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+    cfg.blockDim = dim3(kWriterThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = static_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t lr = cudaLaunchKernelEx(&cfg, mla_kv_write_kernel, static_cast<uint8_t*>(kv.data), kv.num_slots,
+                                              kv.row_bytes, slot_idx, static_cast<const uint16_t*>(latent_bf16),
+                                              static_cast<const uint16_t*>(rope_bf16), n_rows, reserved_slot, err);
+    return (lr == cudaSuccess && cudaGetLastError() == cudaSuccess) ? MLA_OK : MLA_ECUDA;
 }

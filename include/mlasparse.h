@@ -106,11 +106,14 @@ typedef struct {
  *   reserved_slot the slot writes must never land in (0 in every caller)
  * Precondition: no two rows of one call name the same non-reserved slot (which
  * of them would land is unspecified).
- * Ordering: the writer lets the next kernel on the stream begin launching while
- * it runs (programmatic dependent launch); only a kernel launched with
- * programmatic stream serialization can start early, and such a kernel must
- * wait for its predecessor (griddepcontrol.wait) before reading the cache, as
- * mla_sparse_decode does. Ordinary launches and copies are ordered as usual.
+ * Ordering: the writer is launched with programmatic stream serialization: its
+ * CTAs may become resident while the previous kernel on the stream finishes, and
+ * they read nothing (slot indices, inputs, cache) until that kernel and its
+ * memory are complete (griddepcontrol.wait). It also lets the next kernel on the
+ * stream begin launching while it runs; only a kernel launched with programmatic
+ * stream serialization can start early, and such a kernel must wait for its
+ * predecessor before reading the cache, as mla_sparse_decode and the writer
+ * itself do. Ordinary launches and copies are ordered as usual.
  * Returns MLA_OK, MLA_EINVAL or MLA_ECUDA.
  */
 int mla_kv_write(mla_kv_cache_t kv, const int64_t* slot_idx, const void* latent_bf16,
