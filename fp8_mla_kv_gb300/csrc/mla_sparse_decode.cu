@@ -96,7 +96,12 @@ struct DecodeArgs {
     const int32_t* block_table; // [n_seq, bt_pages]
     const int32_t* token_seq;   // [T] block-table row of each token, or null (row 0)
     int bt_pages, n_seq, page_size;
-    int T, H, d_qk, W, nsplit, split_len;
+    int T, H, d_qk, W, nsplit;
+    // Splits of a token's list (nsplit > 1): by positions, split_len each, or,
+    // when rank_chunk > 0, by present entries: every CTA of the token compacts
+    // the whole list (W <= kListMax) and keeps an equal share of its present
+    // entries, ceil(count / rank_chunk) shares at most nsplit.
+    int split_len, rank_chunk;
     float sm_scale_log2;   // sm_scale * log2(e)
 };
 
@@ -128,8 +133,10 @@ mla_sparse_decode_kernel(const DecodeArgs args) {
     constexpr uint32_t kRowRead = kRopeOn ? kRowBytes : kNopeReadBytes;
 
     // Launched with programmatic stream serialization: wait for the previous
-    // kernel on the stream (and its memory) before reading any input.
+    // kernel on the stream (and its memory) before reading any input. The
+    // merge of split partials may then start launching; it waits for this grid.
     pdl_wait();
+    pdl_launch_dependents();
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&full[s], 1);
@@ -171,8 +178,9 @@ mla_sparse_decode_kernel(const DecodeArgs args) {
     // ---- 1. compact the present entries of this split's positions (all warps) ----
     // Thread i takes a contiguous run of `per` positions, loaded all at once; one
     // block-wide scan of the per-thread counts places them in position order.
-    const int p0 = split * args.split_len;
-    const int p1 = min(args.W, p0 + args.split_len);
+    const bool by_rank = args.rank_chunk > 0;
+    const int p0 = by_rank ? 0 : split * args.split_len;
+    const int p1 = by_rank ? args.W : min(args.W, p0 + args.split_len);
     const int per = (max(0, p1 - p0) + kThreads - 1) / kThreads;     // <= kPerThread
     const int32_t* trow = args.topk + static_cast<int64_t>(t) * args.W + p0 + threadIdx.x * per;
     const int mine = max(0, min(per, p1 - (p0 + static_cast<int>(threadIdx.x) * per)));
@@ -229,6 +237,13 @@ mla_sparse_decode_kernel(const DecodeArgs args) {
     for (int k = 0; k < kPerThread; ++k)
         if (idxv[k] != 0) list[off++] = idxv[k];
     __syncthreads();
+    int lbase = 0;     // first list entry of this CTA
+    if (by_rank) {
+        const int shares = min(args.nsplit, max(1, (n_valid + args.rank_chunk - 1) / args.rank_chunk));
+        const int len = (n_valid + shares - 1) / shares;
+        lbase = min(n_valid, split * len);
+        n_valid = min(n_valid, lbase + len) - lbase;
+    }
     const int nblk = (n_valid + kNB - 1) / kNB;
 
     if (warp >= kProducer) {
@@ -258,7 +273,7 @@ mla_sparse_decode_kernel(const DecodeArgs args) {
             __syncwarp();
             if (lane < n_b)
                 bulk_g2s(dst + lane * kRowBytes,
-                         args.cache + static_cast<int64_t>(list[b * kNB + lane]) * args.row_bytes, kRowRead, &full[s]);
+                         args.cache + static_cast<int64_t>(list[lbase + b * kNB + lane]) * args.row_bytes, kRowRead, &full[s]);
         }
         if (lane == 0) issued_s[pw] = cnt;
         __syncthreads();     // matches the consumers' final barrier
@@ -508,6 +523,9 @@ mla_sparse_decode_kernel(const DecodeArgs args) {
                 mma_f16(o[4 * qd + 3], pa, b0d, b1d);
             }
         }
+        // The stage is next written by the async proxy (cp.async.bulk): order this
+        // warp's generic reads of it before that write.
+        fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
     }
@@ -572,6 +590,8 @@ mla_sparse_decode_kernel(const DecodeArgs args) {
             if (warp == 0 && c == 0) args.lse[static_cast<int64_t>(t) * H + h] = lse_r[r];
         } else {
             const int64_t prow = (static_cast<int64_t>(t) * args.nsplit + split) * H + h;
+            if (warp == 0 && c == 0) args.ws_lse[prow] = lse_r[r];
+            if (!(lt[r] > 0.0f)) continue;     // lse = -inf: the merge skips this partial's o
             float* orow = args.ws_o + prow * kLatent + 128 * warp + 32 * c;
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
@@ -581,22 +601,33 @@ mla_sparse_decode_kernel(const DecodeArgs args) {
                         make_float4(o[4 * qd + 0][2 * r + e] * mm, o[4 * qd + 1][2 * r + e] * mm,
                                     o[4 * qd + 2][2 * r + e] * mm, o[4 * qd + 3][2 * r + e] * mm);
             }
-            if (warp == 0 && c == 0) args.ws_lse[prow] = lse_r[r];
         }
     }
 }
 
 // Merge of the split partials of one (token, head): lse = ln sum_s exp(lse_s),
-// out = sum_s exp(lse_s - lse) o_s, in split order.
+// out = sum_s exp(lse_s - lse) o_s, in split order. Thread x takes dims 4x ..
+// 4x + 3; the loads of kMergeBatch splits are issued together. Launched with
+// programmatic stream serialization behind the decode, whose grid it waits for.
+constexpr int kMergeBatch = 8;
+
 __global__ void __launch_bounds__(128)
 mla_split_combine_kernel(const float* __restrict__ ws_o, const float* __restrict__ ws_lse,
                          int H, int nsplit, __nv_bfloat16* __restrict__ out, float* __restrict__ lse) {
+    pdl_wait();
     const int64_t th = blockIdx.x;              // t * H + h
     const int64_t t = th / H;
     const int h = static_cast<int>(th % H);
-    float mx = -INFINITY;
-    for (int s = 0; s < nsplit; ++s) mx = fmaxf(mx, ws_lse[(t * nsplit + s) * H + h]);
     const int d = 4 * threadIdx.x;
+    float mx = -INFINITY;
+    for (int s0 = 0; s0 < nsplit; s0 += kMergeBatch) {
+        float ls[kMergeBatch];
+#pragma unroll
+        for (int q = 0; q < kMergeBatch; ++q)
+            ls[q] = (s0 + q < nsplit) ? ws_lse[(t * nsplit + s0 + q) * H + h] : -INFINITY;
+#pragma unroll
+        for (int q = 0; q < kMergeBatch; ++q) mx = fmaxf(mx, ls[q]);
+    }
     __nv_bfloat16* orow = out + th * kLatent + d;
     if (mx == -INFINITY) {
         *reinterpret_cast<uint2*>(orow) = make_uint2(0u, 0u);
@@ -605,14 +636,26 @@ mla_split_combine_kernel(const float* __restrict__ ws_o, const float* __restrict
     }
     float wsum = 0.0f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int s = 0; s < nsplit; ++s) {
-        const int64_t prow = (t * nsplit + s) * H + h;
-        const float ls = ws_lse[prow];
-        if (ls == -INFINITY) continue;
-        const float w = expf(ls - mx);
-        wsum += w;
-        const float4 v = *reinterpret_cast<const float4*>(ws_o + prow * kLatent + d);
-        acc.x += w * v.x; acc.y += w * v.y; acc.z += w * v.z; acc.w += w * v.w;
+    for (int s0 = 0; s0 < nsplit; s0 += kMergeBatch) {
+        float ls[kMergeBatch];
+        float4 v[kMergeBatch];
+#pragma unroll
+        for (int q = 0; q < kMergeBatch; ++q) {
+            const int64_t prow = (t * nsplit + min(s0 + q, nsplit - 1)) * H + h;
+            ls[q] = (s0 + q < nsplit) ? ws_lse[prow] : -INFINITY;
+            // A split with no present entry (lse -inf) left its o unwritten.
+            v[q] = (ls[q] == -INFINITY) ? make_float4(0.f, 0.f, 0.f, 0.f)
+                                        : *reinterpret_cast<const float4*>(ws_o + prow * kLatent + d);
+        }
+#pragma unroll
+        for (int q = 0; q < kMergeBatch; ++q) {
+            const float w = (ls[q] == -INFINITY) ? 0.0f : expf(ls[q] - mx);
+            wsum += w;
+            acc.x = fmaf(w, v[q].x, acc.x);
+            acc.y = fmaf(w, v[q].y, acc.y);
+            acc.z = fmaf(w, v[q].z, acc.z);
+            acc.w = fmaf(w, v[q].w, acc.w);
+        }
     }
     const float inv = 1.0f / wsum;
     *reinterpret_cast<uint2*>(orow) = make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv),
@@ -622,22 +665,35 @@ mla_split_combine_kernel(const float* __restrict__ ws_o, const float* __restrict
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Number of splits of each token's top-k list. A CTA's row rate is set by its
-// one copy-issuing warp, and a split costs a partial write, a merge and one more
-// prologue, so a token's list is split only when there are fewer (token, head
-// group) pairs than SMs; then into enough pieces for about two CTAs per SM,
-// each of at least 64 positions. At most kListMax positions per split.
+// Number of splits of each token's top-k list. A split costs a partial write, a
+// merge and one more prologue, so a token's list is split only when there are
+// fewer (token, head group) pairs than SMs; then into enough pieces for about
+// kSplitCtasPerSm CTAs per SM, each of at least kSplitMinRows positions, and at
+// most kListMax positions per split.
+constexpr int kSplitCtasPerSm = 2;
+constexpr int kSplitMinRows = 64;
+
 int choose_nsplit(int T, int H, int W, int sms) {
     if (T <= 0 || W <= 0) return 1;
     const int64_t base = static_cast<int64_t>(T) * ((H + kHeads - 1) / kHeads);
     int64_t ns = 1;
-    if (base < sms) ns = (2ll * sms + base - 1) / base;
-    const int64_t max_ns = (W >= 64) ? W / 64 : 1;
+    if (base < sms) ns = (static_cast<int64_t>(kSplitCtasPerSm) * sms + base - 1) / base;
+    const int64_t max_ns = (W >= kSplitMinRows) ? W / kSplitMinRows : 1;
     if (ns > max_ns) ns = max_ns;
     const int64_t min_ns = (W + kListMax - 1) / kListMax;
     if (ns < min_ns) ns = min_ns;
     if (ns < 1) ns = 1;
     return static_cast<int>(ns);
+}
+
+// Lists that one CTA can compact are split by present entries, so that a list
+// whose entries are all in its first positions (a short sequence in a wide
+// buffer) still spreads over as many CTAs as it has rows for: a list of c
+// present entries takes ceil(c / rank_chunk) CTAs, and the CTAs left over exit
+// after the compaction. Longer lists are split by positions.
+int rank_chunk_for(int W, int nsplit) {
+    if (nsplit <= 1 || W > kListMax) return 0;
+    return (W + nsplit - 1) / nsplit;
 }
 
 size_t workspace_for(int T, int H, int nsplit) {
@@ -710,6 +766,7 @@ int launch_decode(const void* q_bf16, int T, int H, int d_qk, mla_kv_cache_t kv,
     a.page_size = pg.page_size;
     a.T = T; a.H = H; a.d_qk = d_qk; a.W = W; a.nsplit = nsplit;
     a.split_len = (W + nsplit - 1) / nsplit;
+    a.rank_chunk = rank_chunk_for(W, nsplit);
     a.sm_scale_log2 = sm_scale * kLog2e;
     const dim3 grid(static_cast<unsigned>(static_cast<int64_t>(T) * ((H + kHeads - 1) / kHeads)), static_cast<unsigned>(nsplit));
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -727,9 +784,16 @@ int launch_decode(const void* q_bf16, int T, int H, int d_qk, mla_kv_cache_t kv,
                                                      : cudaLaunchKernelEx(&cfg, mla_sparse_decode_kernel<false>, a);
     if (lr != cudaSuccess || cudaGetLastError() != cudaSuccess) return MLA_ECUDA;
     if (nsplit > 1) {
-        mla_split_combine_kernel<<<static_cast<unsigned>(static_cast<int64_t>(T) * H), 128, 0, st>>>(
-            a.ws_o, a.ws_lse, H, nsplit, a.out, a.lse);
-        if (cudaGetLastError() != cudaSuccess) return MLA_ECUDA;
+        cudaLaunchConfig_t mcfg = {};
+        mcfg.gridDim = dim3(static_cast<unsigned>(static_cast<int64_t>(T) * H));
+        mcfg.blockDim = dim3(128);
+        mcfg.stream = st;
+        mcfg.attrs = attr;
+        mcfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&mcfg, mla_split_combine_kernel, static_cast<const float*>(a.ws_o),
+                               static_cast<const float*>(a.ws_lse), H, nsplit, a.out, a.lse) != cudaSuccess ||
+            cudaGetLastError() != cudaSuccess)
+            return MLA_ECUDA;
     }
     return MLA_OK;
 }

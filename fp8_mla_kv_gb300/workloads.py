@@ -257,8 +257,8 @@ def by_name(name: str, **kw) -> Workload:
 # Reduced variants: same structure, sizes the oracle finishes in seconds.
 SMALL = {
     "tiny": dict(),
-    "nope": dict(num_slots=8192, T=6, W=272, max_len=256),
-    "rope": dict(num_slots=16384, T=3, H=64, W=256),
+    "nope": dict(num_slots=8192, T=6, W=544, max_len=512),
+    "rope": dict(num_slots=16384, T=3, H=64, W=512),
     "prefill": dict(num_pages=64, page=64, T=80, W=64),
     "sweep": dict(num_slots=16384, sizes=(1, 64, 1024), T=4, W=256),
 }

@@ -19,9 +19,9 @@ pytestmark = pytest.mark.gpu
 
 @pytest.mark.parametrize("name", ["tiny", "sweep"])
 def test_writer_then_decode_in_one_graph(name):
-    # tiny: 4 tokens, the list split across CTAs (partials and the merge launch);
-    # sweep: 200 tokens of 256 positions, one CTA per token.
-    wl = workloads.tiny() if name == "tiny" else workloads.sweep(num_slots=16384, sizes=(1, 64, 1024), T=200, W=256)
+    # tiny: 4 tokens of 128 positions, one CTA per token; sweep: 200 tokens of
+    # 512 positions, cut across CTAs (partials and the merge launch).
+    wl = workloads.tiny() if name == "tiny" else workloads.sweep(num_slots=16384, sizes=(1, 64, 1024), T=200, W=512)
     g, c = build_both(wl)
     d = dev()
     db = wl.decode

@@ -1,0 +1,103 @@
+"""The decode's two schedules against the float64 oracle.
+
+Whole units: one CTA per (token, group of 16 heads). Cut units: the work (each
+unit's rows plus a fixed charge per unit) is cut into equal ranges, one per CTA,
+and a unit cut by range ends is merged from its pieces. The lists here are built
+to reach the cut schedule's corners: tokens with no present entry (the unit is
+written by the range that holds its start), one entry, 31 / 32 / 33 entries (a
+block boundary), full lists, present entries scattered among -1 or packed at the
+front, and head counts that leave a short last head group.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from fp8_mla_kv_gb300 import mlasparse as M
+
+from _parity import check_decode, dev
+
+pytestmark = pytest.mark.gpu
+
+NUM_SLOTS = 16384
+
+
+def _cache(seed, nope=False):
+    g = torch.Generator().manual_seed(seed)
+    n = NUM_SLOTS - 1
+    slots = torch.arange(1, NUM_SLOTS, dtype=torch.int64)
+    lat = torch.randn((n, 512), generator=g).to(torch.bfloat16)
+    rope = None if nope else torch.randn((n, 64), generator=g).to(torch.bfloat16)
+    gc = torch.zeros((NUM_SLOTS, 656), dtype=torch.uint8, device=dev())
+    M.mla_kv_write(gc, slots.to(dev()), lat.to(dev()), None if rope is None else rope.to(dev()))
+    cc = np.zeros((NUM_SLOTS, 656), np.uint8)
+    oracle.kv_write(cc, slots.numpy(), lat, rope)
+    torch.cuda.synchronize()
+    return gc, cc
+
+
+def _topk(counts, W, seed):
+    g = torch.Generator().manual_seed(seed)
+    rows = []
+    for t, cnt in enumerate(counts):
+        row = torch.full((W,), -1, dtype=torch.int32)
+        pick = (torch.randperm(NUM_SLOTS - 1, generator=g)[:cnt] + 1).to(torch.int32)
+        if t % 2:
+            row[torch.randperm(W, generator=g)[:cnt]] = pick       # scattered among -1
+        else:
+            row[:cnt] = pick                                        # packed at the front
+        rows.append(row)
+    return torch.stack(rows)
+
+
+def _run(counts, H, W, seed, d_qk=576, tokens=None):
+    gc, cc = _cache(seed, nope=(d_qk == 512))
+    T = len(counts)
+    g = torch.Generator().manual_seed(seed + 1)
+    q = torch.randn((T, H, d_qk), generator=g).to(torch.bfloat16)
+    topk = _topk(counts, W, seed + 2)
+    sm = 1.0 / d_qk ** 0.5
+    out, lse = M.mla_sparse_decode(q.to(dev()), gc, topk.to(dev()), sm)
+    torch.cuda.synchronize()
+    assert M.mla_get_error() == 0
+    ro, rl, bad = oracle.sparse_decode(q, cc, topk.numpy(), sm, tokens=tokens)
+    assert bad == 0
+    check_decode(out, lse, ro, rl, tokens=tokens)
+    return q, gc, topk, sm, out, lse
+
+
+def test_cut_units_with_empty_short_and_full_lists():
+    counts = [0, 1, 31, 32, 33, 1024, 500, 0, 2, 777] * 4
+    q, gc, topk, sm, out, lse = _run(counts, 16, 1024, seed=21)
+    # Same inputs again: the merge order is fixed, so the result is bit-identical.
+    out2, lse2 = M.mla_sparse_decode(q.to(dev()), gc, topk.to(dev()), sm)
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
+    assert torch.equal(lse.view(torch.int32), lse2.view(torch.int32))
+
+
+def test_cut_units_with_a_short_last_head_group():
+    # H = 20: head groups of 16 and 4; the second group's q block holds 4 heads.
+    _run([2000, 0, 1500, 3, 999], 20, 2000, seed=22)
+
+
+def test_cut_units_nope_rows():
+    _run([900, 450, 1, 0, 64, 899, 300], 16, 900, seed=23, d_qk=512)
+
+
+def test_cut_units_many_tokens_sampled():
+    # 300 tokens with random counts: more units than CTAs, ranges holding many
+    # short units; compared on a sample of tokens.
+    rng = np.random.default_rng(24)
+    counts = rng.integers(0, 601, size=300).tolist()
+    counts[:3] = [0, 0, 0]
+    tokens = sorted(set(rng.choice(300, 50, replace=False).tolist()) | {0, 1, 2, 299})
+    _run(counts, 16, 600, seed=24, tokens=tokens)
+
+
+def test_whole_units_many_tokens_sampled():
+    # 1,300 tokens: at least four units per CTA slot, so one CTA per unit.
+    rng = np.random.default_rng(25)
+    counts = rng.integers(0, 700, size=1300).tolist()
+    tokens = sorted(set(rng.choice(1300, 40, replace=False).tolist()) | {0, 1299})
+    _run(counts, 16, 700, seed=25, tokens=tokens)

@@ -71,7 +71,7 @@ def test_nope_structure():
     wl = workloads.small("nope")
     topk = wl.decode.topk.numpy()
     lens = (topk >= 0).sum(1)
-    assert (lens >= 1).all() and (lens <= 256).all()
+    assert (lens >= 1).all() and (lens <= 512).all()
     for row, n in zip(topk, lens):
         assert (row[:n] > 0).all() and (row[n:] == -1).all()     # active prefix, -1 tail
     _present_rows_distinct(wl.decode.topk, wl.num_slots)
