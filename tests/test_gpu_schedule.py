@@ -1,11 +1,10 @@
-"""The decode's two schedules against the float64 oracle.
+"""The decode's work split against the float64 oracle.
 
-Whole units: one CTA per (token, group of 16 heads). Cut units: the work (each
-unit's rows plus a fixed charge per unit) is cut into equal ranges, one per CTA,
-and a unit cut by range ends is merged from its pieces. The lists here are built
-to reach the cut schedule's corners: tokens with no present entry (the unit is
-written by the range that holds its start), one entry, 31 / 32 / 33 entries (a
-block boundary), full lists, present entries scattered among -1 or packed at the
+With fewer (token, head group) units than the GPU has SMs, each token's list is
+split across CTAs by present entries and the partials merged; with more units,
+one CTA takes one unit whole. The lists here are built to reach the corners of
+both: tokens with no present entry, one entry, 31 / 32 / 33 entries (a block
+boundary), full lists, present entries scattered among -1 or packed at the
 front, and head counts that leave a short last head group.
 """
 import numpy as np
@@ -66,7 +65,7 @@ def _run(counts, H, W, seed, d_qk=576, tokens=None):
     return q, gc, topk, sm, out, lse
 
 
-def test_cut_units_with_empty_short_and_full_lists():
+def test_split_lists_with_empty_short_and_full_lists():
     counts = [0, 1, 31, 32, 33, 1024, 500, 0, 2, 777] * 4
     q, gc, topk, sm, out, lse = _run(counts, 16, 1024, seed=21)
     # Same inputs again: the merge order is fixed, so the result is bit-identical.
@@ -76,18 +75,18 @@ def test_cut_units_with_empty_short_and_full_lists():
     assert torch.equal(lse.view(torch.int32), lse2.view(torch.int32))
 
 
-def test_cut_units_with_a_short_last_head_group():
-    # H = 20: head groups of 16 and 4; the second group's q block holds 4 heads.
+def test_split_lists_with_a_short_last_head_group():
+    # H = 20: head groups of 16 and 4.
     _run([2000, 0, 1500, 3, 999], 20, 2000, seed=22)
 
 
-def test_cut_units_nope_rows():
+def test_split_lists_nope_rows():
     _run([900, 450, 1, 0, 64, 899, 300], 16, 900, seed=23, d_qk=512)
 
 
-def test_cut_units_many_tokens_sampled():
-    # 300 tokens with random counts: more units than CTAs, ranges holding many
-    # short units; compared on a sample of tokens.
+def test_many_units_random_counts_sampled():
+    # 300 tokens with random counts: more units than SMs, one CTA per unit;
+    # compared on a sample of tokens.
     rng = np.random.default_rng(24)
     counts = rng.integers(0, 601, size=300).tolist()
     counts[:3] = [0, 0, 0]
@@ -96,7 +95,7 @@ def test_cut_units_many_tokens_sampled():
 
 
 def test_whole_units_many_tokens_sampled():
-    # 1,300 tokens: at least four units per CTA slot, so one CTA per unit.
+    # 1,300 tokens of 700 positions, one CTA per unit.
     rng = np.random.default_rng(25)
     counts = rng.integers(0, 700, size=1300).tolist()
     tokens = sorted(set(rng.choice(1300, 40, replace=False).tolist()) | {0, 1299})
