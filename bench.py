@@ -179,6 +179,11 @@ WORKLOADS = {
     "sweep-small": (lambda: workloads.sweep(num_slots=262144, T=256),
                     "reduced sweep for profiling: 262,144-slot cache (172 MB); 8,192-row padded write; decode "
                     "T=256, H=16, top-k 2,048 (the full sweep's launch shape)"),
+    # reduced RoPE decode for section captures: the full launch shape (512 CTAs)
+    # over a 262,144-slot cache (172 MB > L2)
+    "rope-small": (lambda: workloads.rope(num_slots=262144),
+                   "reduced RoPE decode for profiling: 262,144-slot cache (172 MB), T=128, H=64, d_qk=576, "
+                   "top-k 2,048 (the full RoPE launch shape)"),
     "nope": (lambda: workloads.nope(),
              "NoPE decode: 131,072-slot cache, T=64, H=16, d_qk=512, W=2,176, active length U(1..2048)"),
     "rope": (lambda: workloads.rope(),
