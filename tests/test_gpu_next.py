@@ -180,14 +180,15 @@ def test_upconvert_full_size():
     assert M.mla_get_error() == 0
 
 
-def test_paged_with_head_groups_and_splits_equals_physical():
+@pytest.mark.parametrize("page", [16, 4])
+def test_paged_with_head_groups_and_splits_equals_physical(page):
     """H = 64 (four head groups) and T = 3 (the list is split): an identity block
-    table gives exactly the physical-slot decode."""
+    table gives exactly the physical-slot decode, with 16-slot pages (a 1,024-page
+    table) and 4-slot pages (4,096)."""
     wl = workloads.small("rope")
     g, _ = build_both(wl)
     db = wl.decode
     d = dev()
-    page = 16
     bt = torch.arange(wl.num_slots // page, dtype=torch.int32, device=d)
     ref_out, ref_lse = gpu_decode(g, db)
     out, lse = M.mla_sparse_decode_paged(db.q.to(d), g, db.topk.to(d), bt, page, db.sm_scale)
