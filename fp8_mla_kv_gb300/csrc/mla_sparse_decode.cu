@@ -668,10 +668,12 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 // Number of splits of each token's top-k list. A split costs a partial write, a
 // merge and one more prologue, so a token's list is split only when there are
 // fewer (token, head group) pairs than SMs; then into enough pieces for about
-// kSplitCtasPerSm CTAs per SM, each of at least kSplitMinRows positions, and at
+// kSplitCtasPerSm CTAs per SM, each of at least kSplitMinRows positions (a
+// shorter piece saves less loop time than the merge launch costs: the 4-token,
+// 128-position case runs 13.4 us unsplit against 15.5 us in two pieces), and at
 // most kListMax positions per split.
 constexpr int kSplitCtasPerSm = 2;
-constexpr int kSplitMinRows = 64;
+constexpr int kSplitMinRows = 256;
 
 int choose_nsplit(int T, int H, int W, int sms) {
     if (T <= 0 || W <= 0) return 1;

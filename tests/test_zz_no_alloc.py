@@ -102,12 +102,12 @@ def test_noalloc_runs_small_shapes_and_rejects_large_ones():
     torch.cuda.set_device(dev)
     wl, cache = _nope_inputs(dev)
     g = torch.Generator().manual_seed(99)
-    T, H, W = 1, 16, 128
+    T, H, W = 1, 16, 512
     need = M.mla_sparse_decode_workspace_bytes(T, H, W)
     assert 0 < need <= SCRATCH_BYTES
     q = torch.randn((T, H, 512), generator=g).to(torch.bfloat16).to(dev)
     slots = torch.randperm(wl.num_slots - 1, generator=g)[:W].to(torch.int32) + 1
-    slots[100:] = -1
+    slots[300:] = -1
     topk = slots.view(T, W).to(dev)
     ref_out, ref_lse = M.mla_sparse_decode(q, cache, topk, 0.05)
     torch.cuda.synchronize()
