@@ -121,10 +121,14 @@ mla_sparse_decode_kernel(const DecodeArgs args) {
     uint64_t* empty = full + kStages;
     int* issued_s = reinterpret_cast<int*>(empty + kStages);
 
-    // blockIdx.x = t * head_groups + hg: the head groups of a token run side by
-    // side and gather the same rows, so all but the first read them from L2.
+    // blockIdx.x = (T - 1 - t) * head_groups + hg: the head groups of a token run
+    // side by side and gather the same rows, so all but the first read them from
+    // L2; tokens are taken from the last to the first, because in a causal
+    // (prefill-shaped) batch the later tokens have the longest lists and starting
+    // them first shortens the tail (the prefill shape: 103.6 us against 111.7 in
+    // token order). No result depends on the order.
     const int head_groups = (args.H + kHeads - 1) / kHeads;
-    const int t = static_cast<int>(blockIdx.x / head_groups);
+    const int t = args.T - 1 - static_cast<int>(blockIdx.x / head_groups);
     const int hg = static_cast<int>(blockIdx.x % head_groups);
     const int split = blockIdx.y;
     const int warp = threadIdx.x >> 5;
