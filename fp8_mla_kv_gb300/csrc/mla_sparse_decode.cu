@@ -8,8 +8,12 @@
 // shared memory, so -1, slot 0 and out-of-range indices are never dereferenced.
 //
 // Work decomposition: one CTA per (token, split of the top-k list, group of 16
-// heads), the head groups of a token adjacent in launch order; 4 consumer warps
-// and 2 producer warps. Every thread loads a contiguous run of the split's
+// heads), the head groups of a token adjacent in launch order and tokens taken
+// from the last to the first; 4 consumer warps and 2 producer warps. A token's
+// list is split only when there are fewer (token, head group) pairs than SMs;
+// lists that one CTA can compact are then split by present entries (each CTA of
+// the token compacts the whole list and keeps an equal share of what is
+// present), longer ones by positions. Every thread loads a contiguous run of the
 // positions at once (the q loads are issued before them), maps them through the
 // block table when the list holds sequence positions (the paged entry point,
 // vLLM PR #55277, Purpose item 2), and one block-wide scan places the
@@ -39,8 +43,11 @@
 //         What does not need P (sigma, O's rescale when it moves, the f16 pairs
 //         scale_row / sigma, the first V rows) is done before the barriers, off
 //         the path from P to the first PV MMA.
+// A consumer warp releases a stage only after fencing the async proxy, since the
+// next write to the stage is a bulk copy and its own reads were generic loads.
 // Splits write a normalised partial (o, lse) to the caller's workspace and a
-// second kernel merges them in split order (deterministic: no float atomics).
+// second kernel, launched with programmatic stream serialization, merges them in
+// split order (deterministic: no float atomics).
 #include <cfloat>
 #include <climits>
 #include <cmath>
