@@ -1,0 +1,77 @@
+"""The decode replayed many times in a CUDA graph must give the same bits every
+time, whatever the outputs and the workspace held before each replay.
+
+Each replay overwrites the outputs with NaN first, and the workspace with 0xFF or
+0x00 bytes, so that a result read before it was written, a partial merged before
+it was complete, or a stage of the copy ring overwritten while a warp still reads
+it shows up as a NaN or as a changed bit. Back-to-back replays keep the copy ring
+and the merge under the same timing pressure as a serving loop."""
+import pytest
+import torch
+
+from fp8_mla_kv_gb300 import mlasparse as M
+from fp8_mla_kv_gb300 import workloads
+
+from _parity import build_both, dev
+
+pytestmark = pytest.mark.gpu
+
+REPLAYS = 24
+
+
+@pytest.mark.parametrize("name", ["nope", "rope", "sweep"])
+def test_graph_replays_are_bit_stable(name):
+    wl = workloads.small(name)
+    g, _ = build_both(wl)
+    d = dev()
+    db = wl.decode
+    q, topk = db.q.to(d), db.topk.to(d)
+    ws = M.alloc_workspace(db.T, db.H, db.W, d)
+    ref_out, ref_lse = M.mla_sparse_decode(q, g, topk, db.sm_scale, workspace=ws)
+    torch.cuda.synchronize()
+    assert M.mla_get_error() == 0
+    out = torch.empty_like(ref_out)
+    lse = torch.empty_like(ref_lse)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        M.mla_sparse_decode(q, g, topk, db.sm_scale, out=out, lse=lse, workspace=ws)
+    for i in range(REPLAYS):
+        out.fill_(float("nan"))
+        lse.fill_(float("nan"))
+        if ws is not None:
+            ws.fill_(0xFF if i % 2 == 0 else 0x00)
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out.view(torch.int16), ref_out.view(torch.int16)), f"replay {i}"
+        assert torch.equal(lse.view(torch.int32), ref_lse.view(torch.int32)), f"replay {i}"
+    assert M.mla_get_error() == 0
+
+
+def test_back_to_back_replays_are_bit_stable():
+    # Ten decodes in one graph, no host synchronisation in between: each call's
+    # merge overlaps the next call's launch.
+    wl = workloads.small("nope")
+    g, _ = build_both(wl)
+    d = dev()
+    db = wl.decode
+    q, topk = db.q.to(d), db.topk.to(d)
+    ws = M.alloc_workspace(db.T, db.H, db.W, d)
+    assert ws is not None, "the reduced NoPE lists are split, so the merge runs"
+    ref_out, ref_lse = M.mla_sparse_decode(q, g, topk, db.sm_scale, workspace=ws)
+    torch.cuda.synchronize()
+    outs = [torch.full_like(ref_out, float("nan")) for _ in range(10)]
+    lses = [torch.full_like(ref_lse, float("nan")) for _ in range(10)]
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for o, l in zip(outs, lses):
+            M.mla_sparse_decode(q, g, topk, db.sm_scale, out=o, lse=l, workspace=ws)
+    for _ in range(4):
+        for o, l in zip(outs, lses):
+            o.fill_(float("nan"))
+            l.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        for o, l in zip(outs, lses):
+            assert torch.equal(o.view(torch.int16), ref_out.view(torch.int16))
+            assert torch.equal(l.view(torch.int32), ref_lse.view(torch.int32))
+    assert M.mla_get_error() == 0
