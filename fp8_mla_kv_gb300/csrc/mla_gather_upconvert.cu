@@ -184,6 +184,9 @@ mla_gather_upconvert_kernel(const uint8_t* __restrict__ cache, int64_t num_slots
             st_v4(orow + 16 * lane + 8, make_uint4(o[4], o[5], o[6], o[7]));
             if (lane < 8) st_v4(orow + kLatent + 8 * lane, tail);
         }
+        // The stage is next written by the async proxy (cp.async.bulk): order this
+        // warp's generic reads of it before that write.
+        fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
     }
