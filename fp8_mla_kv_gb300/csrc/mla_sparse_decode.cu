@@ -143,6 +143,24 @@ mla_sparse_decode_kernel(const DecodeArgs args) {
     const int H = args.H;
     constexpr uint32_t kRowRead = kRopeOn ? kRowBytes : kNopeReadBytes;
 
+    // The positions this CTA compacts (all of the token's list when it is split
+    // by present entries).
+    const bool by_rank = args.rank_chunk > 0;
+    const int p0 = by_rank ? 0 : split * args.split_len;
+    const int p1 = by_rank ? args.W : min(args.W, p0 + args.split_len);
+    // While the previous kernel on the stream may still be running, bring those
+    // positions and this head group's q rows into L2. A prefetch returns nothing
+    // to the kernel; every load after the wait below sees the previous kernel's
+    // writes.
+    {
+        const char* lb = reinterpret_cast<const char*>(args.topk + static_cast<int64_t>(t) * args.W + p0);
+        const int lines = (max(0, p1 - p0) * 4 + 127) / 128;
+        for (int i = threadIdx.x; i < lines; i += kThreads) prefetch_l2(lb + 128 * i);
+        const int nh = min(kHeads, args.H - hg * kHeads);
+        const char* qb = reinterpret_cast<const char*>(args.q + (static_cast<int64_t>(t) * args.H + hg * kHeads) * args.d_qk);
+        const int qlines = (nh * args.d_qk * 2 + 127) / 128;
+        for (int i = threadIdx.x; i < qlines; i += kThreads) prefetch_l2(qb + 128 * i);
+    }
     // Launched with programmatic stream serialization: wait for the previous
     // kernel on the stream (and its memory) before reading any input. The
     // merge of split partials may then start launching; it waits for this grid.
@@ -189,9 +207,6 @@ mla_sparse_decode_kernel(const DecodeArgs args) {
     // ---- 1. compact the present entries of this split's positions (all warps) ----
     // Thread i takes a contiguous run of `per` positions, loaded all at once; one
     // block-wide scan of the per-thread counts places them in position order.
-    const bool by_rank = args.rank_chunk > 0;
-    const int p0 = by_rank ? 0 : split * args.split_len;
-    const int p1 = by_rank ? args.W : min(args.W, p0 + args.split_len);
     const int per = (max(0, p1 - p0) + kThreads - 1) / kThreads;     // <= kPerThread
     const int32_t* trow = args.topk + static_cast<int64_t>(t) * args.W + p0 + threadIdx.x * per;
     const int mine = max(0, min(per, p1 - (p0 + static_cast<int>(threadIdx.x) * per)));
