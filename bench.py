@@ -245,8 +245,8 @@ def decode_figures(db, num_slots, t_s, row_read=None):
 
 def measure_configs(dev, flush):
     """The four other configurations: decode timed by graph replay with L2 flushed
-    before each replay (median), plus the 528-byte rows (NoPE) and the paged entry
-    point (prefill)."""
+    before each replay (median), plus the 528-byte rows (NoPE), the paged entry
+    point and the token-pair prefill kernel (prefill)."""
     from fp8_mla_kv_gb300 import mlasparse as M
     res = {}
     for name in ("tiny", "nope", "rope", "prefill"):
@@ -276,6 +276,12 @@ def measure_configs(dev, flush):
             tp = time_graph(flush, lambda: M.mla_sparse_decode_paged(q, cache, pos, bt, wl.page_size, db.sm_scale,
                                                                      out=out, lse=lse, workspace=ws))
             rec["paged"] = decode_figures(db, wl.num_slots, tp)
+            # The token-pair prefill kernel on the same batch (physical and paged).
+            tk2 = time_graph(flush, lambda: M.mla_sparse_prefill(q, cache, tk, db.sm_scale, out=out, lse=lse))
+            rec["prefill_kernel"] = decode_figures(db, wl.num_slots, tk2)
+            tk2p = time_graph(flush, lambda: M.mla_sparse_prefill_paged(q, cache, pos, bt, wl.page_size, db.sm_scale,
+                                                                         out=out, lse=lse))
+            rec["prefill_kernel_paged"] = decode_figures(db, wl.num_slots, tk2p)
         res[name] = rec
         del cache, q, tk, out, lse, ws
         torch.cuda.synchronize()

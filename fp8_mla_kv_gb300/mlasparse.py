@@ -29,7 +29,8 @@ MLA_ERR_PIPELINE_TIMEOUT = 0x4
 MLA_ERR_GATHER_INDEX_RANGE = 0x8
 
 SYMBOLS = ("mla_kv_write", "mla_sparse_decode", "mla_sparse_decode_workspace_bytes",
-           "mla_sparse_decode_paged", "mla_gather_upconvert", "mla_get_error", "mla_strerror")
+           "mla_sparse_decode_paged", "mla_sparse_prefill", "mla_sparse_prefill_paged",
+           "mla_gather_upconvert", "mla_get_error", "mla_strerror")
 
 
 class MlaError(RuntimeError):
@@ -70,6 +71,13 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
                                                     c.c_int, c.c_void_p, c.c_int, c.c_int, c.c_void_p, c.c_int,
                                                     c.c_float, c.c_void_p, c.c_void_p, c.c_void_p, c.c_size_t,
                                                     c.c_void_p]
+            lib.mla_sparse_prefill.restype = c.c_int
+            lib.mla_sparse_prefill.argtypes = [c.c_void_p, c.c_int, c.c_int, c.c_int, KVCache, c.c_void_p,
+                                               c.c_int, c.c_float, c.c_void_p, c.c_void_p, c.c_void_p]
+            lib.mla_sparse_prefill_paged.restype = c.c_int
+            lib.mla_sparse_prefill_paged.argtypes = [c.c_void_p, c.c_int, c.c_int, c.c_int, KVCache, c.c_void_p,
+                                                     c.c_int, c.c_void_p, c.c_int, c.c_int, c.c_void_p, c.c_int,
+                                                     c.c_float, c.c_void_p, c.c_void_p, c.c_void_p]
             lib.mla_gather_upconvert.restype = c.c_int
             lib.mla_gather_upconvert.argtypes = [KVCache, c.c_void_p, c.c_int64, c.c_int, c.c_void_p, c.c_void_p]
             lib.mla_get_error.restype = c.c_int
@@ -190,6 +198,56 @@ def mla_sparse_decode_paged(q: torch.Tensor, cache: torch.Tensor, topk_pos: torc
                                         _stream(stream))
     if rc != MLA_OK:
         raise MlaError(rc, "mla_sparse_decode_paged")
+    return out, lse
+
+
+def mla_sparse_prefill(q: torch.Tensor, cache: torch.Tensor, topk_idx: torch.Tensor, sm_scale: float,
+                       out: torch.Tensor | None = None, lse: torch.Tensor | None = None, stream=None):
+    """What mla_sparse_decode computes, by token pairs that share their rows (causal
+    prefill): q bf16 [T, H, d_qk]; topk int32 [T, W] with W <= 2304; returns
+    (out bf16 [T, H, 512], lse fp32 [T, H]). No workspace."""
+    _require_cuda(q, cache, topk_idx)
+    T, H, d_qk = (int(s) for s in q.shape)
+    W = int(topk_idx.shape[1])
+    assert q.dtype == torch.bfloat16 and q.is_contiguous()
+    assert topk_idx.dtype == torch.int32 and topk_idx.is_contiguous() and topk_idx.shape[0] == T
+    if out is None:
+        out = torch.empty((T, H, 512), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((T, H), dtype=torch.float32, device=q.device)
+    rc = load().mla_sparse_prefill(q.data_ptr(), T, H, d_qk, kv_cache(cache), topk_idx.data_ptr(), W,
+                                   float(sm_scale), out.data_ptr(), lse.data_ptr(), _stream(stream))
+    if rc != MLA_OK:
+        raise MlaError(rc, "mla_sparse_prefill")
+    return out, lse
+
+
+def mla_sparse_prefill_paged(q: torch.Tensor, cache: torch.Tensor, topk_pos: torch.Tensor,
+                             block_table: torch.Tensor, page_size: int, sm_scale: float,
+                             token_seq: torch.Tensor | None = None, out: torch.Tensor | None = None,
+                             lse: torch.Tensor | None = None, stream=None):
+    """mla_sparse_prefill with the top-k given as sequence positions through a block
+    table (arguments as mla_sparse_decode_paged, no workspace)."""
+    _require_cuda(q, cache, topk_pos, block_table, token_seq)
+    T, H, d_qk = (int(s) for s in q.shape)
+    W = int(topk_pos.shape[1])
+    bt = block_table if block_table.dim() == 2 else block_table.view(1, -1)
+    assert q.dtype == torch.bfloat16 and q.is_contiguous()
+    assert topk_pos.dtype == torch.int32 and topk_pos.is_contiguous() and topk_pos.shape[0] == T
+    assert bt.dtype == torch.int32 and bt.is_contiguous()
+    if token_seq is not None:
+        assert token_seq.dtype == torch.int32 and token_seq.is_contiguous() and token_seq.numel() == T
+    if out is None:
+        out = torch.empty((T, H, 512), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((T, H), dtype=torch.float32, device=q.device)
+    rc = load().mla_sparse_prefill_paged(q.data_ptr(), T, H, d_qk, kv_cache(cache), topk_pos.data_ptr(), W,
+                                         bt.data_ptr(), int(bt.shape[0]), int(bt.shape[1]),
+                                         token_seq.data_ptr() if token_seq is not None else None,
+                                         int(page_size), float(sm_scale), out.data_ptr(), lse.data_ptr(),
+                                         _stream(stream))
+    if rc != MLA_OK:
+        raise MlaError(rc, "mla_sparse_prefill_paged")
     return out, lse
 
 

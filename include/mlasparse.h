@@ -199,6 +199,44 @@ int mla_sparse_decode_paged(const void* q_bf16, int T, int H, int d_qk, mla_kv_c
                             void* stream);
 
 /*
+ * mla_sparse_prefill - what mla_sparse_decode computes, for batches whose
+ * adjacent tokens share most of their top-k rows (a causal prefill: token i's
+ * list is nearly a subset of token i+1's).
+ *
+ * The pages route prefill-sized batches to a dedicated kernel (sglang PR
+ * #39288, Motivation: above 64 query rows the prefill kernel runs) and note
+ * that the decode kernel also serves prefill today (sglang PR #47013, Speed
+ * Tests). Here one CTA takes tokens 2u and 2u+1 with one group of 16 heads; the
+ * rows present in both lists are copied and converted once for both tokens.
+ * A row present in one list only is computed for that token only, so the result
+ * of every token is exactly the decode statement of mla_sparse_decode over its
+ * own list (same masking rules, bit-identical whatever slot 0 holds); only the
+ * order of accumulation differs from mla_sparse_decode, so the two agree to
+ * rounding, not bit for bit. A slot listed twice counts twice, as in the decode.
+ *
+ * Arguments as mla_sparse_decode, without the workspace; W is at most 2304
+ * (MLA_EUNSUPPORTED otherwise). Batches whose adjacent tokens share few rows
+ * compute correctly but gain nothing; batches of fewer than about two tokens
+ * per SM leave SMs idle (no list is split): use mla_sparse_decode for those.
+ * Launched with programmatic stream serialization like the decode.
+ * Returns MLA_OK, MLA_EINVAL, MLA_EUNSUPPORTED or MLA_ECUDA.
+ */
+int mla_sparse_prefill(const void* q_bf16, int T, int H, int d_qk, mla_kv_cache_t kv,
+                       const int32_t* topk_idx, int W, float sm_scale, void* out_bf16, float* lse,
+                       void* stream);
+
+/*
+ * mla_sparse_prefill_paged - mla_sparse_prefill with the top-k list given as
+ * sequence positions and a block table, mapped exactly as in
+ * mla_sparse_decode_paged (vLLM PR #55277, Purpose item 2). Arguments as
+ * mla_sparse_decode_paged, without the workspace.
+ */
+int mla_sparse_prefill_paged(const void* q_bf16, int T, int H, int d_qk, mla_kv_cache_t kv,
+                             const int32_t* topk_pos, int W, const int32_t* block_table, int n_seq,
+                             int max_pages, const int32_t* token_seq, int page_size, float sm_scale,
+                             void* out_bf16, float* lse, void* stream);
+
+/*
  * mla_gather_upconvert - gather rows of the cache and widen them to BF16
  * (vLLM PR #55277, Changes table: cp_gather_and_upconvert_fp8_kv_cache, the
  * chunked-context path; the NoPE tail is written as exact zeros).

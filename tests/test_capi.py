@@ -67,5 +67,17 @@ def test_host_validation_without_gpu(lib):
     for ps, bt, nseq, mp in ((0, 16, 1, 4), (64, None, 1, 4), (64, 16, 0, 4), (64, 16, 1, 0)):
         assert lib.mla_sparse_decode_paged(None, 1, 16, 576, kv, None, 8, bt, nseq, mp, None, ps, 0.1,
                                            None, None, None, 0, None) == M.MLA_EINVAL
+    # prefill: same checks as the decode, and W past one CTA's list is refused
+    pf = lib.mla_sparse_prefill
+    assert pf(None, 1, 16, 300, kv, None, 8, 0.1, None, None, None) == M.MLA_EUNSUPPORTED
+    assert pf(None, 1, 129, 576, kv, None, 8, 0.1, None, None, None) == M.MLA_EUNSUPPORTED
+    assert pf(None, 1, 16, 576, kv, None, 2305, 0.1, None, None, None) == M.MLA_EUNSUPPORTED
+    assert pf(None, 1, 16, 576, kv, None, 8, float("inf"), None, None, None) == M.MLA_EINVAL
+    assert pf(None, 0, 16, 576, kv, None, 8, 0.1, None, None, None) == M.MLA_OK
+    assert pf(None, 2, 16, 576, kv, None, 8, 0.1, None, None, None) == M.MLA_EINVAL
+    assert pf(None, 1, 16, 576, kv528, None, 8, 0.1, None, None, None) == M.MLA_EUNSUPPORTED
+    for ps, bt, nseq, mp in ((0, 16, 1, 4), (64, None, 1, 4), (64, 16, 0, 4), (64, 16, 1, 0)):
+        assert lib.mla_sparse_prefill_paged(None, 1, 16, 576, kv, None, 8, bt, nseq, mp, None, ps, 0.1,
+                                            None, None, None) == M.MLA_EINVAL
     for code in (0, -1, -2, -3, -4):
         assert lib.mla_strerror(code)

@@ -75,3 +75,27 @@ def test_back_to_back_replays_are_bit_stable():
             assert torch.equal(o.view(torch.int16), ref_out.view(torch.int16))
             assert torch.equal(l.view(torch.int32), ref_lse.view(torch.int32))
     assert M.mla_get_error() == 0
+
+
+def test_prefill_graph_replays_are_bit_stable():
+    wl = workloads.small("prefill")
+    g, _ = build_both(wl)
+    d = dev()
+    db = wl.decode
+    q, topk = db.q.to(d), db.topk.to(d)
+    ref_out, ref_lse = M.mla_sparse_prefill(q, g, topk, db.sm_scale)
+    torch.cuda.synchronize()
+    out = torch.empty_like(ref_out)
+    lse = torch.empty_like(ref_lse)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for _ in range(3):
+            M.mla_sparse_prefill(q, g, topk, db.sm_scale, out=out, lse=lse)
+    for i in range(REPLAYS):
+        out.fill_(float("nan"))
+        lse.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out.view(torch.int16), ref_out.view(torch.int16)), f"replay {i}"
+        assert torch.equal(lse.view(torch.int32), ref_lse.view(torch.int32)), f"replay {i}"
+    assert M.mla_get_error() == 0

@@ -10,7 +10,8 @@ rescaling paths, which random N(0,1) inputs reach almost only on the first rows:
 * mixed magnitudes: tile scales spread over many octaves inside one list and
   inside one row.
 
-Each case is checked with the decode tolerance of the other parity tests
+Each case runs through the decode and through the token-pair prefill kernel,
+and is checked with the decode tolerance of the other parity tests
 (max|out-ref| <= 1e-2 max|ref| + 1e-3, |lse-ref| <= 1e-3). The same check per
 (token, head) row against that row's own max|ref| is printed as a diagnostic, and
 asserted (within 2e-2) where the row scales span at most 2^12: the PV operand is
@@ -48,8 +49,11 @@ def _write_rows(latent_f32, rope_f32):
     return g, c
 
 
-def _run(g, c, q, topk, sm_scale, per_row_rtol=None, label=""):
-    out, lse = M.mla_sparse_decode(q.to(dev()), g, topk.to(dev()), sm_scale)
+ENTRIES = {"decode": M.mla_sparse_decode, "prefill": M.mla_sparse_prefill}
+
+
+def _run(g, c, q, topk, sm_scale, per_row_rtol=None, label="", entry="decode"):
+    out, lse = ENTRIES[entry](q.to(dev()), g, topk.to(dev()), sm_scale)
     torch.cuda.synchronize()
     ro, rl, bad = oracle.sparse_decode(q, c, topk.numpy(), sm_scale)
     assert bad == 0
@@ -79,8 +83,9 @@ def _topk(T, W, n, perm_seed=None):
     return torch.stack(rows)
 
 
+@pytest.mark.parametrize("entry", ["decode", "prefill"])
 @pytest.mark.parametrize("d_qk", [576, 512])
-def test_rising_scores_and_scales_move_every_block(d_qk):
+def test_rising_scores_and_scales_move_every_block(d_qk, entry):
     # Row j = a_j * v + small noise with a_j rising: its score against q = beta_h v
     # rises by about 20 log2 units per 32 rows (heads with beta_h > 0), its tile
     # scales rise with it. Heads with beta_h < 0 see falling scores instead.
@@ -100,10 +105,11 @@ def test_rising_scores_and_scales_move_every_block(d_qk):
     topk = _topk(T, 1024, n)
     topk[1, :n] = torch.flip(topk[1, :n], [0])                              # falling order
     topk[2, :n] = topk[2, :n][torch.randperm(n, generator=gen)]              # random order
-    _run(g, c, q, topk, 1.0 / d_qk ** 0.5, per_row_rtol=2e-2, label=f"rising d_qk={d_qk}")
+    _run(g, c, q, topk, 1.0 / d_qk ** 0.5, per_row_rtol=2e-2, label=f"rising d_qk={d_qk} {entry}", entry=entry)
 
 
-def test_scales_growing_along_the_list():
+@pytest.mark.parametrize("entry", ["decode", "prefill"])
+def test_scales_growing_along_the_list(entry):
     # Row magnitudes grow geometrically (2^-11 .. 1) along the list with random
     # directions: sigma, the running maximum of the tile scales, is raised over
     # and over while the scores stay moderate.
@@ -115,10 +121,11 @@ def test_scales_growing_along_the_list():
     g, c = _write_rows(lat, rope)
     q = (4.0 * torch.randn((T, H, 576), generator=gen)).to(torch.bfloat16)
     topk = _topk(T, 768, n)
-    _run(g, c, q, topk, 1.0 / 24.0, per_row_rtol=2e-2, label="growing scales")
+    _run(g, c, q, topk, 1.0 / 24.0, per_row_rtol=2e-2, label=f"growing scales {entry}", entry=entry)
 
 
-def test_tile_scales_spanning_many_octaves():
+@pytest.mark.parametrize("entry", ["decode", "prefill"])
+def test_tile_scales_spanning_many_octaves(entry):
     # Each tile of each row gets its own magnitude 2^-e, e uniform in 0..30, so a
     # list mixes tile scales from about 2^-39 to 2^-8 (scale = amax / 448).
     gen = torch.Generator().manual_seed(13)
@@ -129,10 +136,11 @@ def test_tile_scales_spanning_many_octaves():
     g, c = _write_rows(lat, rope)
     q = (8.0 * torch.randn((T, H, 576), generator=gen)).to(torch.bfloat16)
     topk = _topk(T, 1024, n, perm_seed=5)
-    _run(g, c, q, topk, 1.0 / 24.0, label="2^-30..1 tile magnitudes")
+    _run(g, c, q, topk, 1.0 / 24.0, label=f"2^-30..1 tile magnitudes {entry}", entry=entry)
 
 
-def test_tile_scales_spanning_twelve_octaves_per_row_check():
+@pytest.mark.parametrize("entry", ["decode", "prefill"])
+def test_tile_scales_spanning_twelve_octaves_per_row_check(entry):
     gen = torch.Generator().manual_seed(14)
     n, T, H = 900, 3, 16
     e = torch.randint(0, 13, (n, 4), generator=gen).float()
@@ -141,4 +149,4 @@ def test_tile_scales_spanning_twelve_octaves_per_row_check():
     g, c = _write_rows(lat, rope)
     q = (2.0 * torch.randn((T, H, 576), generator=gen)).to(torch.bfloat16)
     topk = _topk(T, 1024, n, perm_seed=9)
-    _run(g, c, q, topk, 1.0 / 24.0, per_row_rtol=2e-2, label="2^-12..1 tile magnitudes")
+    _run(g, c, q, topk, 1.0 / 24.0, per_row_rtol=2e-2, label=f"2^-12..1 tile magnitudes {entry}", entry=entry)
