@@ -333,8 +333,17 @@ def run_ours(args, rank, world, local_rank):
     q_d, topk_d = db.q.to(dev), db.topk.to(dev)
     out_d = torch.empty((db.T, db.H, 512), dtype=torch.bfloat16, device=dev)
     lse_d = torch.empty((db.T, db.H), dtype=torch.float32, device=dev)
-    ws = M.alloc_workspace(db.T, db.H, db.W, dev)
+    use_prefill = args.kernel == "prefill"
+    ws = None if use_prefill else M.alloc_workspace(db.T, db.H, db.W, dev)
     launches_per_step = (1 if wb is not None else 0) + 1 + (1 if ws is not None else 0)   # per timed step
+
+    def attend(qd, tkd, o, l, w):
+        # The attention call of the step: the per-token decode, or the token-pair
+        # prefill kernel (--kernel prefill; same result, no workspace).
+        if use_prefill:
+            M.mla_sparse_prefill(qd, cache, tkd, db.sm_scale, out=o, lse=l)
+        else:
+            M.mla_sparse_decode(qd, cache, tkd, db.sm_scale, out=o, lse=l, workspace=w)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
 
@@ -344,7 +353,7 @@ def run_ours(args, rank, world, local_rank):
 
     def step():
         write()
-        M.mla_sparse_decode(q_d, cache, topk_d, db.sm_scale, out=out_d, lse=lse_d, workspace=ws)
+        attend(q_d, topk_d, out_d, lse_d, ws)
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -363,7 +372,7 @@ def run_ours(args, rank, world, local_rank):
         with torch.cuda.graph(g_write):
             write()
     with torch.cuda.graph(g_decode):
-        M.mla_sparse_decode(q_d, cache, topk_d, db.sm_scale, out=out_d, lse=lse_d, workspace=ws)
+        attend(q_d, topk_d, out_d, lse_d, ws)
     for _ in range(3):
         flush.zero_()
         g_step.replay()
@@ -521,8 +530,7 @@ def run_ours(args, rank, world, local_rank):
             d = d_ins[i]
             if wb is not None:
                 M.mla_kv_write(cache, d[0], d[1], d[2] if len(w_in) == 3 else None)
-            M.mla_sparse_decode(d[-2], cache, d[-1], db.sm_scale, out=d_outs[i][0], lse=d_outs[i][1],
-                                workspace=ws2[i])
+            attend(d[-2], d[-1], d_outs[i][0], d_outs[i][1], ws2[i])
             ev_done[i].record(xs)
             s_out.wait_event(ev_done[i])
             with torch.cuda.stream(s_out):
@@ -585,6 +593,7 @@ def run_ours(args, rank, world, local_rank):
                 "workload": wl_desc,
                 "T": db.T, "H": db.H, "d_qk": db.d_qk, "topk": db.W, "num_slots": wl.num_slots,
                 "present_entries": n_valid,
+                "attention_call": "mla_sparse_prefill" if use_prefill else "mla_sparse_decode",
                 "writer_rows": n_rows, "writer_rows_written": n_written,
                 "l2": "flushed between timed steps (256 MiB write, outside the timed events)",
                 "timing": "CUDA-graph replay of the whole step (writer + decode in one graph); CUDA events on "
@@ -609,7 +618,7 @@ def run_ours(args, rank, world, local_rank):
                 "hbm_frac": writer_alg / (writer_ms * 1e-3) / 1e9 / peak,
             },
             "roofline": {
-                "kernel": "mla_sparse_decode_kernel (+ split combine)",
+                "kernel": "mla_sparse_pair_kernel" if use_prefill else "mla_sparse_decode_kernel (+ split combine)",
                 "bound": "hbm",
                 "achieved": achieved,
                 "peak": peak,
@@ -617,7 +626,7 @@ def run_ours(args, rank, world, local_rank):
                 "frac": achieved / peak,
                 "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)" if peak_kind == "measured" else "fallback 6.8 TB/s",
                 "algorithmic_bytes_per_launch": decode_alg,
-                "traffic": traffic if args.workload == "sweep" else None,
+                "traffic": traffic if args.workload == "sweep" and not use_prefill else None,
             },
             "clocks": clocks,
             "e2e": {
@@ -689,6 +698,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-configs", action="store_true")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="sweep")
+    ap.add_argument("--kernel", choices=["decode", "prefill"], default="decode",
+                    help="attention call of the step: mla_sparse_decode or the token-pair mla_sparse_prefill")
     args = ap.parse_args()
     rank, world, local_rank = dist_env()
     if args.impl == "reference":
