@@ -35,7 +35,8 @@ def _sources():
 
 
 def _deps():
-    return _sources() + glob.glob(os.path.join(CSRC, "*.cuh")) + [os.path.join(ROOT, "include", "mlasparse.h")]
+    # The source directory itself: adding or removing a translation unit changes its mtime.
+    return _sources() + glob.glob(os.path.join(CSRC, "*.cuh")) + [os.path.join(ROOT, "include", "mlasparse.h"), CSRC]
 
 
 def up_to_date() -> bool:
