@@ -588,9 +588,15 @@ mla_sparse_decode_kernel(const DecodeArgs args) {
         lt[0] += lsum_s[w * kHeads + g];
         lt[1] += lsum_s[w * kHeads + g + 8];
     }
-    const float mult[2] = {lt[0] > 0.0f ? sigma / lt[0] : 0.0f, lt[1] > 0.0f ? sigma / lt[1] : 0.0f};
-    const float lse_r[2] = {lt[0] > 0.0f ? (m_ref[0] + log2f(lt[0])) * kLn2 : -INFINITY,
-                            lt[1] > 0.0f ? (m_ref[1] + log2f(lt[1])) * kLn2 : -INFINITY};
+    // l = 0: nothing present (out 0, lse -inf). l NaN: a listed row holds a NaN
+    // (out and lse NaN, as the decode statement gives).
+    const float kNaN = __int_as_float(0x7FC00000);
+    float mult[2], lse_r[2];
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+        mult[r] = lt[r] > 0.0f ? sigma / lt[r] : (lt[r] == 0.0f ? 0.0f : kNaN);
+        lse_r[r] = lt[r] > 0.0f ? (m_ref[r] + log2f(lt[r])) * kLn2 : (lt[r] == 0.0f ? -INFINITY : kNaN);
+    }
     const int hs[2] = {h_lo, h_hi};
     // Thread (g, c) holds, for head row r, dims 128w + 32c + 16e + 4q + i in
     // o[4q + i][2r + e]: 32 contiguous output values per head row.
@@ -617,7 +623,7 @@ mla_sparse_decode_kernel(const DecodeArgs args) {
         } else {
             const int64_t prow = (static_cast<int64_t>(t) * args.nsplit + split) * H + h;
             if (warp == 0 && c == 0) args.ws_lse[prow] = lse_r[r];
-            if (!(lt[r] > 0.0f)) continue;     // lse = -inf: the merge skips this partial's o
+            if (lt[r] == 0.0f) continue;       // lse = -inf: the merge skips this partial's o
             float* orow = args.ws_o + prow * kLatent + 128 * warp + 32 * c;
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
@@ -632,7 +638,7 @@ mla_sparse_decode_kernel(const DecodeArgs args) {
 }
 
 // Merge of the split partials of one (token, head): lse = ln sum_s exp(lse_s),
-// out = sum_s exp(lse_s - lse) o_s, in split order. Thread x takes dims 4x ..
+// out = sum_s exp(lse_s - lse) o_s, in split order; a NaN partial makes both NaN. Thread x takes dims 4x ..
 // 4x + 3; the loads of kMergeBatch splits are issued together. Launched with
 // programmatic stream serialization behind the decode, whose grid it waits for.
 constexpr int kMergeBatch = 8;
@@ -646,15 +652,26 @@ mla_split_combine_kernel(const float* __restrict__ ws_o, const float* __restrict
     const int h = static_cast<int>(th % H);
     const int d = 4 * threadIdx.x;
     float mx = -INFINITY;
+    bool nan = false;
     for (int s0 = 0; s0 < nsplit; s0 += kMergeBatch) {
         float ls[kMergeBatch];
 #pragma unroll
         for (int q = 0; q < kMergeBatch; ++q)
             ls[q] = (s0 + q < nsplit) ? ws_lse[(t * nsplit + s0 + q) * H + h] : -INFINITY;
 #pragma unroll
-        for (int q = 0; q < kMergeBatch; ++q) mx = fmaxf(mx, ls[q]);
+        for (int q = 0; q < kMergeBatch; ++q) {
+            mx = fmaxf(mx, ls[q]);
+            nan = nan || ls[q] != ls[q];
+        }
     }
     __nv_bfloat16* orow = out + th * kLatent + d;
+    if (nan) {
+        // A split met a NaN row: the whole result is NaN, as unsplit.
+        const uint32_t qn = pack_bf16x2(__int_as_float(0x7FC00000), __int_as_float(0x7FC00000));
+        *reinterpret_cast<uint2*>(orow) = make_uint2(qn, qn);
+        if (threadIdx.x == 0) lse[th] = __int_as_float(0x7FC00000);
+        return;
+    }
     if (mx == -INFINITY) {
         *reinterpret_cast<uint2*>(orow) = make_uint2(0u, 0u);
         if (threadIdx.x == 0) lse[th] = -INFINITY;

@@ -809,7 +809,8 @@ mla_sparse_pair_kernel(const PairArgs args) {
             float lt = 0.0f;
 #pragma unroll
             for (int nt = 0; nt < 4; ++nt) lt += lsum_s[(j * 4 + nt) * kHeads + g + 8 * r];
-            const float mm = lt > 0.0f ? sigma[j] / lt : 0.0f;
+            // l = 0: nothing present (out 0, lse -inf); l NaN: a listed row holds a NaN.
+            const float mm = lt > 0.0f ? sigma[j] / lt : (lt == 0.0f ? 0.0f : __int_as_float(0x7FC00000));
             // Thread (g, c) holds, for head row r, dims 64w + 16c + 8e + 4q + i in
             // o[j][4q + i][2r + e]: 16 contiguous output values per head row.
             __nv_bfloat16* orow = args.out + (static_cast<int64_t>(tok[j]) * H + h) * kLatent + 64 * warp + 16 * c;
@@ -824,7 +825,7 @@ mla_sparse_pair_kernel(const PairArgs args) {
             }
             if (warp == 0 && c == 0)
                 args.lse[static_cast<int64_t>(tok[j]) * H + h] =
-                    lt > 0.0f ? (m_ref[j][r] + log2f(lt)) * kLn2 : -INFINITY;
+                    lt > 0.0f ? (m_ref[j][r] + log2f(lt)) * kLn2 : (lt == 0.0f ? -INFINITY : __int_as_float(0x7FC00000));
         }
     }
 }

@@ -182,3 +182,42 @@ def test_many_tokens():
     ro, rl, _ = oracle.sparse_decode(db.q, c, db.topk.numpy(), db.sm_scale, tokens=tokens)
     check_decode(out, lse, ro, rl, tokens=tokens)
     assert M.mla_get_error() == 0
+
+
+@pytest.mark.parametrize("T,W,n_valid", [(2, 1024, 900), (160, 128, 100)])
+def test_nan_row_makes_the_tokens_that_list_it_nan(T, W, n_valid):
+    # A row written from NaN latent values holds E4M3 NaN codes. A token that
+    # lists it gets NaN out and NaN lse, as the decode statement (and the oracle)
+    # gives, whether its list is split across CTAs (first case: 2 tokens, split by
+    # present entries, partials merged) or not (second case); the other tokens
+    # are untouched.
+    gen = torch.Generator().manual_seed(51)
+    n = 2000
+    lat = torch.randn((n, 512), generator=gen)
+    lat[7] = float("nan")                                  # slot 8
+    lat = lat.to(torch.bfloat16)
+    rope = torch.randn((n, 64), generator=gen).to(torch.bfloat16)
+    slots = torch.arange(1, n + 1, dtype=torch.int64)
+    g = torch.zeros((4096, 656), dtype=torch.uint8, device=dev())
+    M.mla_kv_write(g, slots.to(dev()), lat.to(dev()), rope.to(dev()))
+    c = np.zeros((4096, 656), np.uint8)
+    oracle.kv_write(c, slots.numpy(), lat, rope)
+    topk = torch.full((T, W), -1, dtype=torch.int32)
+    for t in range(T):
+        pick = torch.randperm(n, generator=gen)[:n_valid] + 1
+        pick = pick[pick != 8]
+        if t % 2 == 0:
+            pick[int(torch.randint(0, pick.numel(), (1,), generator=gen))] = 8
+        topk[t, :pick.numel()] = pick.to(torch.int32)
+    q = torch.randn((T, 16, 576), generator=gen).to(torch.bfloat16)
+    if T == 2:
+        assert M.mla_sparse_decode_workspace_bytes(T, 16, W) > 0, "this case is meant to split"
+    out, lse = M.mla_sparse_decode(q.to(dev()), g, topk.to(dev()), 1.0 / 24.0)
+    torch.cuda.synchronize()
+    assert M.mla_get_error() == 0
+    even, odd = list(range(0, T, 2)), list(range(1, T, 2))
+    o, l = out.float().cpu(), lse.cpu()
+    assert torch.isnan(o[even]).all() and torch.isnan(l[even]).all()
+    ro, rl, _ = oracle.sparse_decode(q, c, topk.numpy(), 1.0 / 24.0, tokens=odd)
+    assert np.isnan(oracle.sparse_decode(q, c, topk.numpy(), 1.0 / 24.0, tokens=even[:1])[1][even[0]]).all()
+    check_decode(out, lse, ro, rl, tokens=odd)
