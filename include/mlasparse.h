@@ -146,8 +146,10 @@ size_t mla_sparse_decode_workspace_bytes(int T, int H, int W);
  *   K_j[d]    = e4m3(byte_d of row) * scale[d / 128]      (V_j = K_j)
  *   out[t,h]  = sum_j softmax(s)_j V_j                     (bf16)
  *   lse[t,h]  = ln sum_j exp(s_j)                          (fp32, natural log)
- * An empty J gives out = 0 and lse = -inf. The result does not depend on the
- * order of the entries nor on what slot 0 holds (bit-identical output).
+ * An empty J gives out = 0 and lse = -inf; a row of J holding a NaN code gives
+ * NaN out and lse for that token, whether or not its list is split. The result
+ * does not depend on the order of the entries nor on what slot 0 holds
+ * (bit-identical output).
  *
  * Arguments:
  *   q_bf16     bf16 [T, H, d_qk] row-major, device, 16-byte aligned

@@ -89,7 +89,6 @@ def _corner_lists(W, seed):
     merge's corners; odd pairs scatter their entries among -1."""
     gen = torch.Generator().manual_seed(seed)
     pool = (torch.randperm(NUM_SLOTS - 1, generator=gen) + 1).to(torch.int32)
-    take = iter(range(0, NUM_SLOTS - 1, 1))
     cursor = [0]
 
     def fresh(n):
@@ -176,7 +175,8 @@ def _nan_cache():
 def test_nan_row_of_one_token_stays_out_of_the_other():
     # Pair 0: the NaN row in the second token's list only; pair 1: in the first
     # token's only; pair 2: in both. A token that does not list the row gets the
-    # oracle's finite result; a token that lists it gets what the decode gives.
+    # oracle's finite result; a token that lists it gets NaN out and lse, as the
+    # decode (and the oracle) give.
     gc, cc, nan_slot = _nan_cache()
     gen = torch.Generator().manual_seed(42)
     W = 256
@@ -200,6 +200,7 @@ def test_nan_row_of_one_token_stays_out_of_the_other():
     o, do = out.float().cpu(), dec_out.float().cpu()
     assert torch.equal(torch.isnan(o), torch.isnan(do))
     assert torch.isnan(o[[1, 2, 4, 5]]).all()
+    assert torch.isnan(lse.cpu()[[1, 2, 4, 5]]).all()
     assert torch.equal(lse.cpu().isneginf(), dec_lse.cpu().isneginf())
     assert torch.equal(lse.cpu().isnan(), dec_lse.cpu().isnan())
 
@@ -253,3 +254,29 @@ def test_nope_rows_of_528_bytes():
     assert torch.equal(a[1].view(torch.int32), b[1].view(torch.int32))
     ro, rl, _ = oracle.sparse_decode(db.q, c, db.topk.numpy(), db.sm_scale)
     check_decode(*b, ro, rl)
+
+
+def test_paged_multi_sequence_holes_and_range():
+    # Tokens of three sequences (a pair may mix two block tables), unassigned
+    # pages, positions past the table (absent and flagged) and repeated positions
+    # (a slot listed twice): the pairs' merged lists against the oracle.
+    wl = workloads.small("sweep")
+    g, c = build_both(wl)
+    rng = np.random.default_rng(4)
+    T, H, W, page, n_seq, max_pages = 7, 16, 96, 16, 3, 40
+    n_pages = wl.num_slots // page
+    bt = rng.integers(1, n_pages, size=(n_seq, max_pages)).astype(np.int32)
+    bt[rng.random(bt.shape) < 0.1] = -1
+    pos = rng.integers(-1, max_pages * page + 40, size=(T, W)).astype(np.int32)
+    seq = rng.integers(0, n_seq, size=T).astype(np.int32)
+    q = torch.from_numpy(rng.standard_normal((T, H, 576)).astype(np.float32)).to(torch.bfloat16)
+    d = dev()
+    M.mla_get_error()
+    out, lse = M.mla_sparse_prefill_paged(q.to(d), g, torch.from_numpy(pos).to(d), torch.from_numpy(bt).to(d),
+                                          page, 0.05, token_seq=torch.from_numpy(seq).to(d))
+    torch.cuda.synchronize()
+    err = M.mla_get_error()
+    phys, bad = oracle.paged_to_physical(pos, bt, page, seq)
+    assert bad > 0 and err == M.MLA_ERR_DECODE_INDEX_RANGE
+    ro, rl, _ = oracle.sparse_decode(q, c, phys, 0.05)
+    check_decode(out, lse, ro, rl)
