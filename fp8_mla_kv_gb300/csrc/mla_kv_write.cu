@@ -22,12 +22,33 @@ using namespace mla;
 
 constexpr int kWriterThreads = 256;   // 8 rows in flight per CTA
 
-__device__ __forceinline__ uint32_t quant2(float x0, float x1, float scale, float rcp, bool fast) {
-    // x / scale rounded to nearest even (the IEEE quotient: the fast form is the
-    // residual-corrected reciprocal product), then round-to-nearest-even E4M3
-    // with saturation.
-    const float2 v = fast ? make_float2(div_by_scale(x0, scale, rcp), div_by_scale(x1, scale, rcp))
-                          : make_float2(__fdiv_rn(x0, scale), __fdiv_rn(x1, scale));
+__device__ __forceinline__ uint64_t f32x2(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+
+// x0 / s and x1 / s rounded to nearest even, by the residual-corrected
+// reciprocal product of div_by_scale computed on both values at once with the
+// packed fp32 pipe (the same IEEE operations per value: q0 = RN(x*y), r = x -
+// q0*s exactly, q = RN(q0 + r*y)), then round-to-nearest-even E4M3 with
+// saturation.
+__device__ __forceinline__ uint32_t quant2_fast(float x0, float x1, uint64_t y2, uint64_t ns2) {
+    const uint64_t x = f32x2(x0, x1);
+    uint64_t q0, r, q;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(q0) : "l"(x), "l"(y2));
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(q0), "l"(ns2), "l"(x));
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(q) : "l"(r), "l"(y2), "l"(q0));
+    float q_lo, q_hi;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(q_lo), "=f"(q_hi) : "l"(q));
+    const float2 v = make_float2(copysignf(q_lo, x0), copysignf(q_hi, x1));   // a zero quotient keeps x's sign
+    return static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(v, __NV_SATFINITE, __NV_E4M3));
+}
+
+// The same with the IEEE division, for a tile whose scale is outside the range
+// where the residual above is exact.
+__device__ __forceinline__ uint32_t quant2_ieee(float x0, float x1, float scale) {
+    const float2 v = make_float2(__fdiv_rn(x0, scale), __fdiv_rn(x1, scale));
     return static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(v, __NV_SATFINITE, __NV_E4M3));
 }
 
@@ -78,11 +99,27 @@ mla_kv_write_kernel(uint8_t* __restrict__ cache, int64_t num_slots, int64_t row_
         const bool fast = scale >= kDivFastMin && scale <= kDivFastMax;   // false only for extreme tiles
         const float rcp = __frcp_rn(scale);
 
+        // One branch for the whole warp: every tile of the row in the fast range
+        // (the rule), or the IEEE division on the tiles that are not.
         uint32_t qv[4];
+        if (__all_sync(0xffffffffu, fast)) {
+            const uint64_t y2 = f32x2(rcp, rcp), ns2 = f32x2(-scale, -scale);
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-            qv[k] = quant2(v[4 * k], v[4 * k + 1], scale, rcp, fast) |
-                    (quant2(v[4 * k + 2], v[4 * k + 3], scale, rcp, fast) << 16);
+            for (int k = 0; k < 4; ++k)
+                qv[k] = quant2_fast(v[4 * k], v[4 * k + 1], y2, ns2) |
+                        (quant2_fast(v[4 * k + 2], v[4 * k + 3], y2, ns2) << 16);
+        } else {
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                qv[k] = fast ? (static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(
+                                    make_float2(div_by_scale(v[4 * k], scale, rcp), div_by_scale(v[4 * k + 1], scale, rcp)),
+                                    __NV_SATFINITE, __NV_E4M3)) |
+                                (static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(
+                                    make_float2(div_by_scale(v[4 * k + 2], scale, rcp), div_by_scale(v[4 * k + 3], scale, rcp)),
+                                    __NV_SATFINITE, __NV_E4M3)) << 16))
+                             : (quant2_ieee(v[4 * k], v[4 * k + 1], scale) |
+                                (quant2_ieee(v[4 * k + 2], v[4 * k + 3], scale) << 16));
+        }
 
         uint8_t* row = cache + slot * row_bytes;
         st_v4(row + 16 * lane, make_uint4(qv[0], qv[1], qv[2], qv[3]));
