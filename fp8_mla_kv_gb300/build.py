@@ -36,7 +36,7 @@ def _sources():
 
 def _deps():
     # The source directory itself: adding or removing a translation unit changes its mtime.
-    return _sources() + glob.glob(os.path.join(CSRC, "*.cuh")) + [os.path.join(ROOT, "include", "mlasparse.h"), CSRC]
+    return _sources() + glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(CSRC, "*.h")) + [os.path.join(ROOT, "include", "mlasparse.h"), CSRC]
 
 
 def up_to_date() -> bool:
