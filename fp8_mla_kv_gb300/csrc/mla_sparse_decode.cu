@@ -53,7 +53,6 @@
 #include <cmath>
 
 #include "mla_device.cuh"
-#include "mla_decode_internal.h"
 
 namespace {
 
@@ -742,13 +741,6 @@ int rank_chunk_for(int W, int nsplit) {
     return (W + nsplit - 1) / nsplit;
 }
 
-// Head counts that are a multiple of 64 run on the 64-head tcgen05 kernel, whose
-// CTAs hold a whole SM each; the others on the 16-head kernel.
-bool use_h64(int H) { return H % 64 == 0; }
-int decode_nsplit(int T, int H, int W, int sms) {
-    return use_h64(H) ? mla_host::choose_nsplit_h64(T, H, W, sms) : choose_nsplit(T, H, W, sms);
-}
-
 size_t workspace_for(int T, int H, int nsplit) {
     if (nsplit <= 1) return 0;
     const size_t rows = static_cast<size_t>(T) * nsplit * H;
@@ -762,30 +754,10 @@ extern "C" size_t mla_sparse_decode_workspace_bytes(int T, int H, int W) {
     if (T <= 0 || H <= 0 || H > 128 || W < 0) return 0;
     const int sms = mla_host::sm_count();
     if (sms <= 0) return 0;
-    return workspace_for(T, H, decode_nsplit(T, H, W, sms));
+    return workspace_for(T, H, choose_nsplit(T, H, W, sms));
 }
 
 namespace {
-
-// The merge of split partials, launched with programmatic stream serialization
-// behind the decode (it waits for the decode grid before reading).
-int launch_merge(const float* ws_o, const float* ws_lse, int T, int H, int nsplit, void* out, float* lse,
-                 cudaStream_t st) {
-    cudaLaunchConfig_t mcfg = {};
-    mcfg.gridDim = dim3(static_cast<unsigned>(static_cast<int64_t>(T) * H));
-    mcfg.blockDim = dim3(128);
-    mcfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    mcfg.attrs = attr;
-    mcfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&mcfg, mla_split_combine_kernel, ws_o, ws_lse, H, nsplit,
-                           static_cast<__nv_bfloat16*>(out), lse) != cudaSuccess ||
-        cudaGetLastError() != cudaSuccess)
-        return MLA_ECUDA;
-    return MLA_OK;
-}
 
 struct PageArgs {
     const int32_t* block_table;
@@ -811,40 +783,10 @@ int launch_decode(const void* q_bf16, int T, int H, int d_qk, mla_kv_cache_t kv,
     int* err = mla_host::device_error_word();
     const int sms = mla_host::sm_count();
     if (err == nullptr || sms <= 0) return MLA_ECUDA;
-    const int nsplit = decode_nsplit(T, H, W, sms);
+    const int nsplit = choose_nsplit(T, H, W, sms);
     const size_t need = workspace_for(T, H, nsplit);
     if (need > 0 && (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)))
         return MLA_ENOWORKSPACE;
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    float* ws_o = static_cast<float*>(workspace);
-    float* ws_lse = nsplit > 1 ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
-                                                          static_cast<size_t>(T) * nsplit * H * kLatent * sizeof(float))
-                               : nullptr;
-    if (use_h64(H)) {
-        mla_host::DecodeCall c;
-        c.q = q_bf16;
-        c.cache = static_cast<const uint8_t*>(kv.data);
-        c.topk = topk_idx;
-        c.out = out_bf16;
-        c.lse = lse;
-        c.ws_o = ws_o;
-        c.ws_lse = ws_lse;
-        c.err = err;
-        c.num_slots = kv.num_slots;
-        c.row_bytes = kv.row_bytes;
-        c.block_table = pg.block_table;
-        c.token_seq = pg.token_seq;
-        c.bt_pages = pg.bt_pages;
-        c.n_seq = pg.n_seq;
-        c.page_size = pg.page_size;
-        c.T = T; c.H = H; c.d_qk = d_qk; c.W = W; c.nsplit = nsplit;
-        c.split_len = (W + nsplit - 1) / nsplit;
-        c.rank_chunk = mla_host::rank_chunk_h64(W, nsplit);
-        c.sm_scale_log2 = sm_scale * kLog2e;
-        const int rc = mla_host::launch_decode_h64(c, st);
-        if (rc != MLA_OK) return rc;
-        return nsplit > 1 ? launch_merge(ws_o, ws_lse, T, H, nsplit, out_bf16, lse, st) : MLA_OK;
-    }
 
     if (!mla_host::max_dynamic_smem(reinterpret_cast<const void*>(mla_sparse_decode_kernel<true>), kSmemTotal) ||
         !mla_host::max_dynamic_smem(reinterpret_cast<const void*>(mla_sparse_decode_kernel<false>), kSmemTotal))
@@ -855,8 +797,10 @@ int launch_decode(const void* q_bf16, int T, int H, int d_qk, mla_kv_cache_t kv,
     a.topk = topk_idx;
     a.out = static_cast<__nv_bfloat16*>(out_bf16);
     a.lse = lse;
-    a.ws_o = ws_o;
-    a.ws_lse = ws_lse;
+    a.ws_o = static_cast<float*>(workspace);
+    a.ws_lse = nsplit > 1 ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
+                                                     static_cast<size_t>(T) * nsplit * H * kLatent * sizeof(float))
+                          : nullptr;
     a.err = err;
     a.num_slots = kv.num_slots;
     a.row_bytes = kv.row_bytes;
@@ -870,6 +814,7 @@ int launch_decode(const void* q_bf16, int T, int H, int d_qk, mla_kv_cache_t kv,
     a.rank_chunk = rank_chunk_for(W, nsplit);
     a.sm_scale_log2 = sm_scale * kLog2e;
     const dim3 grid(static_cast<unsigned>(static_cast<int64_t>(T) * ((H + kHeads - 1) / kHeads)), static_cast<unsigned>(nsplit));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = dim3(kThreads);
@@ -883,7 +828,19 @@ int launch_decode(const void* q_bf16, int T, int H, int d_qk, mla_kv_cache_t kv,
     const cudaError_t lr = (d_qk == kLatent + kRope) ? cudaLaunchKernelEx(&cfg, mla_sparse_decode_kernel<true>, a)
                                                      : cudaLaunchKernelEx(&cfg, mla_sparse_decode_kernel<false>, a);
     if (lr != cudaSuccess || cudaGetLastError() != cudaSuccess) return MLA_ECUDA;
-    return nsplit > 1 ? launch_merge(ws_o, ws_lse, T, H, nsplit, out_bf16, lse, st) : MLA_OK;
+    if (nsplit > 1) {
+        cudaLaunchConfig_t mcfg = {};
+        mcfg.gridDim = dim3(static_cast<unsigned>(static_cast<int64_t>(T) * H));
+        mcfg.blockDim = dim3(128);
+        mcfg.stream = st;
+        mcfg.attrs = attr;
+        mcfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&mcfg, mla_split_combine_kernel, static_cast<const float*>(a.ws_o),
+                               static_cast<const float*>(a.ws_lse), H, nsplit, a.out, a.lse) != cudaSuccess ||
+            cudaGetLastError() != cudaSuccess)
+            return MLA_ECUDA;
+    }
+    return MLA_OK;
 }
 
 }  // namespace
