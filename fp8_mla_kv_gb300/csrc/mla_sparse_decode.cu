@@ -166,13 +166,33 @@ mla_sparse_decode_kernel(const DecodeArgs args) {
     // merge of split partials may then start launching; it waits for this grid.
     pdl_wait();
     pdl_launch_dependents();
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], kWarps);
+    // The first copy-issuing warp sets up the ring. When this CTA's first 32
+    // positions are all present slots (unsplit or split by positions, no block
+    // table), they are exactly the first 32 entries of the compacted list, so the
+    // warp copies block 0 right away and the copies land while the whole list is
+    // compacted.
+    bool block0_issued = false;
+    if (warp == kProducer) {
+        if (lane == 0) {
+            for (int s = 0; s < kStages; ++s) {
+                mbar_init(&full[s], 1);
+                mbar_init(&empty[s], kWarps);
+            }
+            issued_s[0] = issued_s[1] = 0;
+            fence_mbar_init();
         }
-        issued_s[0] = issued_s[1] = 0;
-        fence_mbar_init();
+        __syncwarp();
+        if (!by_rank && args.page_size == 0 && p1 - p0 >= kNB) {
+            const int idx = __ldg(args.topk + static_cast<int64_t>(t) * args.W + p0 + lane);
+            const bool present = idx > 0 && static_cast<int64_t>(idx) < args.num_slots;
+            if (__all_sync(0xffffffffu, present)) {
+                if (lane == 0) mbar_arrive_expect_tx(&full[0], kNB * kRowRead);
+                __syncwarp();
+                bulk_g2s(stages + lane * kRowBytes, args.cache + static_cast<int64_t>(idx) * args.row_bytes, kRowRead,
+                         &full[0]);
+                block0_issued = true;
+            }
+        }
     }
 
     // ---- 0. q of this token and head group (consumer warps), loads issued first ----
@@ -277,6 +297,10 @@ mla_sparse_decode_kernel(const DecodeArgs args) {
         // lane j copies row j of the block into the stage ring ----
         const int pw = warp - kProducer;
         int b = pw, cnt = 0;
+        if (block0_issued) {                   // producer 0, block 0 already on its way
+            b += kProducers;
+            cnt = 1;
+        }
         for (; b < nblk; b += kProducers, ++cnt) {
             const int s = b % kStages;
             if (b >= kStages && !mbar_wait_bounded(&empty[s], static_cast<uint32_t>(((b / kStages) - 1) & 1))) {
