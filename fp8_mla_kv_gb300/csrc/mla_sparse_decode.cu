@@ -167,10 +167,10 @@ mla_sparse_decode_kernel(const DecodeArgs args) {
     pdl_wait();
     pdl_launch_dependents();
     // The first copy-issuing warp sets up the ring. When this CTA's first 32
-    // positions are all present slots (unsplit or split by positions, no block
-    // table), they are exactly the first 32 entries of the compacted list, so the
-    // warp copies block 0 right away and the copies land while the whole list is
-    // compacted.
+    // positions are all present (unsplit or split by positions; through the block
+    // table for the paged entry point), they are exactly the first 32 entries of the
+    // compacted list, so the warp copies block 0 right away and the copies land
+    // while the whole list is compacted.
     bool block0_issued = false;
     if (warp == kProducer) {
         if (lane == 0) {
@@ -182,9 +182,21 @@ mla_sparse_decode_kernel(const DecodeArgs args) {
             fence_mbar_init();
         }
         __syncwarp();
-        if (!by_rank && args.page_size == 0 && p1 - p0 >= kNB) {
-            const int idx = __ldg(args.topk + static_cast<int64_t>(t) * args.W + p0 + lane);
-            const bool present = idx > 0 && static_cast<int64_t>(idx) < args.num_slots;
+        if (!by_rank && p1 - p0 >= kNB) {
+            int idx = __ldg(args.topk + static_cast<int64_t>(t) * args.W + p0 + lane);
+            bool present = true;
+            if (args.page_size > 0) {
+                // the same translation as the compaction's; anything it would drop
+                // or flag only turns this shortcut off
+                const int sq = args.token_seq ? __ldg(args.token_seq + t) : 0;
+                const int page = idx >= 0 ? idx / args.page_size : 0;
+                present = idx >= 0 && sq >= 0 && sq < args.n_seq && page < args.bt_pages;
+                const int phys = present ? __ldg(args.block_table + static_cast<int64_t>(sq) * args.bt_pages + page) : -1;
+                const int64_t slot = static_cast<int64_t>(phys) * args.page_size + (idx - page * args.page_size);
+                present = present && phys >= 0 && slot <= INT32_MAX;
+                idx = present ? static_cast<int>(slot) : 0;
+            }
+            present = present && idx > 0 && static_cast<int64_t>(idx) < args.num_slots;
             if (__all_sync(0xffffffffu, present)) {
                 if (lane == 0) mbar_arrive_expect_tx(&full[0], kNB * kRowRead);
                 __syncwarp();
