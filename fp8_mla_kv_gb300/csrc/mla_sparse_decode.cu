@@ -17,7 +17,9 @@
 // positions at once (the q loads are issued before them), maps them through the
 // block table when the list holds sequence positions (the paged entry point,
 // vLLM PR #55277, Purpose item 2), and one block-wide scan places the
-// present slots in a shared-memory list. Rows are 656 bytes, or 528 for a cache
+// present slots in a shared-memory list. When the CTA's first 32 positions are
+// all present, the first copy-issuing warp copies them (block 0) before that, so
+// the first block lands while the list is compacted. Rows are 656 bytes, or 528 for a cache
 // of NoPE rows without a tail (sglang PR #39288, "Relation to other changes"). The
 // producers copy each listed row global -> shared with one cp.async.bulk (656 B,
 // or 528 B for NoPE: the tail is not read) into a 4-stage ring of 32-row blocks,
