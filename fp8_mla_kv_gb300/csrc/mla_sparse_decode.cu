@@ -10,16 +10,20 @@
 // Work decomposition: one CTA per (token, split of the top-k list, group of 16
 // heads), the head groups of a token adjacent in launch order and tokens taken
 // from the last to the first; 4 consumer warps and 2 producer warps. A token's
-// list is split only when there are fewer (token, head group) pairs than SMs;
-// lists that one CTA can compact are then split by present entries (each CTA of
-// the token compacts the whole list and keeps an equal share of what is
-// present), longer ones by positions. Every thread loads a contiguous run of the
-// positions at once (the q loads are issued before them), maps them through the
-// block table when the list holds sequence positions (the paged entry point,
-// vLLM PR #55277, Purpose item 2), and one block-wide scan places the
-// present slots in a shared-memory list. When the CTA's first 32 positions are
-// all present, the first copy-issuing warp copies them (block 0) before that, so
-// the first block lands while the list is compacted. Rows are 656 bytes, or 528 for a cache
+// list is split only when there are fewer (token, head group) pairs than SMs.
+// Lists that one CTA can compact are then split by a plan: a first kernel
+// compacts every token's list once (mla_list_compact_kernel), and each decode
+// CTA reads all tokens' counts and cuts every list into pieces of at most C
+// present entries, C the smallest multiple of 32 (at least kPlanMinRows) for
+// which all pieces fit in one wave of CTAs, so a long list gets more pieces
+// than a short one. Longer lists are split by positions. Every thread loads a
+// contiguous run of the positions at once (the q loads are issued before them),
+// maps them through the block table when the list holds sequence positions (the
+// paged entry point, vLLM PR #55277, Purpose item 2), and one block-wide scan
+// places the present slots in a shared-memory list. When the CTA's first 32
+// positions (or a planned piece's first 32 entries) are all present, the first
+// copy-issuing warp copies them (block 0) before the list is in shared memory,
+// so the first block lands meanwhile. Rows are 656 bytes, or 528 for a cache
 // of NoPE rows without a tail (sglang PR #39288, "Relation to other changes"). The
 // producers copy each listed row global -> shared with one cp.async.bulk (656 B,
 // or 528 B for NoPE: the tail is not read) into a 4-stage ring of 32-row blocks,
@@ -69,6 +73,7 @@ constexpr int kConsumerThreads = kWarps * 32;
 constexpr int kNB = 32;                      // rows per block
 constexpr int kStages = 4;
 constexpr int kListMax = 2304;               // positions one CTA compacts
+constexpr int kPlanMinRows = 128;            // shortest planned piece (fewer partials to merge)
 constexpr int kPerThread = (kListMax + kThreads - 1) / kThreads;   // positions per thread in the compaction
 constexpr int kStageBytes = kNB * kRowBytes; // 20,992
 constexpr int kSmemStages = kStages * kStageBytes;
@@ -95,8 +100,8 @@ struct DecodeArgs {
     const int32_t* topk;
     __nv_bfloat16* out;
     float* lse;
-    float* ws_o;      // [T, nsplit, H, 512] (nsplit > 1)
-    float* ws_lse;    // [T, nsplit, H]
+    float* ws_o;      // [T * nsplit, H, 512], or [plan_pieces, H, 512] when planned
+    float* ws_lse;    // [T * nsplit, H], or [plan_pieces, H]
     int* err;
     int64_t num_slots;
     int64_t row_bytes;          // 656, or 528 (NoPE rows without a tail)
@@ -106,15 +111,59 @@ struct DecodeArgs {
     const int32_t* token_seq;   // [T] block-table row of each token, or null (row 0)
     int bt_pages, n_seq, page_size;
     int T, H, d_qk, W, nsplit;
-    // Splits of a token's list (nsplit > 1): by positions, split_len each, or,
-    // when rank_chunk > 0, by present entries: every CTA of the token compacts
-    // the whole list (W <= kListMax) and keeps an equal share of its present
-    // entries, ceil(count / rank_chunk) shares at most nsplit.
-    int split_len, rank_chunk;
+    // Split of a token's list by positions (nsplit > 1, no plan): split_len each.
+    int split_len;
+    // Planned split (plan_list != nullptr, W <= kListMax): the compacted lists,
+    // their lengths, and per token its first piece and piece count (written by
+    // the decode for the merge); plan_pieces piece slots per head group.
+    int32_t* plan_list;    // [T, W]
+    int32_t* plan_count;   // [T]
+    int2* plan_tok;        // [T]
+    int plan_pieces;
     float sm_scale_log2;   // sm_scale * log2(e)
 };
 
-template <bool kRopeOn>
+__device__ __forceinline__ int warp_sum(int v) {
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) v += __shfl_xor_sync(0xffffffffu, v, d);
+    return v;
+}
+
+// Position -> slot through the block table (vLLM PR #55277, Purpose item 2): a
+// negative position or an unassigned (negative) page is absent (-1); a position
+// past the table, or any position of a token whose sequence row is out of range,
+// is absent and flagged.
+__device__ __forceinline__ int paged_slot(const DecodeArgs& a, const int32_t* bt, bool seq_ok, int pos) {
+    if (pos < 0) return -1;
+    const int page = pos / a.page_size;
+    if (!seq_ok || page >= a.bt_pages) {
+        atomicOr(a.err, MLA_ERR_DECODE_INDEX_RANGE);
+        return -1;
+    }
+    const int phys = __ldg(bt + page);
+    const int64_t slot = static_cast<int64_t>(phys) * a.page_size + (pos - page * a.page_size);
+    return (phys < 0) ? -1 : static_cast<int>(min(slot, static_cast<int64_t>(INT32_MAX)));
+}
+
+// Chunk length of the planned split, from the T list lengths in cnt (one warp,
+// every lane gets the result): the smallest multiple of kNB, at least
+// kPlanMinRows and at least total / G, for which the pieces
+// sum_t max(1, ceil(n_t / C)) number at most G. T <= G, so C = kListMax (one
+// piece per token) always fits and ends the search.
+__device__ __forceinline__ int plan_chunk(const int* cnt, int T, int G, int lane) {
+    int total = 0;
+    for (int i = lane; i < T; i += 32) total += cnt[i];
+    total = warp_sum(total);
+    int C = max(kPlanMinRows, ((total + G - 1) / G + kNB - 1) / kNB * kNB);
+    for (; C < kListMax; C += kNB) {
+        int pieces = 0;
+        for (int i = lane; i < T; i += 32) pieces += max(1, (cnt[i] + C - 1) / C);
+        if (warp_sum(pieces) <= G) break;
+    }
+    return min(C, kListMax);
+}
+
+template <bool kRopeOn, bool kPlanned>
 __global__ void __launch_bounds__(kThreads, 2)
 mla_sparse_decode_kernel(const DecodeArgs args) {
     extern __shared__ __align__(128) uint8_t smem[];
@@ -135,26 +184,26 @@ mla_sparse_decode_kernel(const DecodeArgs args) {
     // L2; tokens are taken from the last to the first, because in a causal
     // (prefill-shaped) batch the later tokens have the longest lists and starting
     // them first shortens the tail (the prefill shape: 103.6 us against 111.7 in
-    // token order). No result depends on the order.
+    // token order). No result depends on the order. A planned split has
+    // blockIdx.x = piece * head_groups + hg; the piece's token comes from the plan.
+    constexpr bool planned = kPlanned;   // args.plan_list != nullptr
     const int head_groups = (args.H + kHeads - 1) / kHeads;
-    const int t = args.T - 1 - static_cast<int>(blockIdx.x / head_groups);
+    int t = planned ? 0 : args.T - 1 - static_cast<int>(blockIdx.x / head_groups);
     const int hg = static_cast<int>(blockIdx.x % head_groups);
-    const int split = blockIdx.y;
+    const int split = planned ? static_cast<int>(blockIdx.x / head_groups) : static_cast<int>(blockIdx.y);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int H = args.H;
     constexpr uint32_t kRowRead = kRopeOn ? kRowBytes : kNopeReadBytes;
 
-    // The positions this CTA compacts (all of the token's list when it is split
-    // by present entries).
-    const bool by_rank = args.rank_chunk > 0;
-    const int p0 = by_rank ? 0 : split * args.split_len;
-    const int p1 = by_rank ? args.W : min(args.W, p0 + args.split_len);
+    // The positions this CTA compacts (none when planned).
+    const int p0 = planned ? 0 : split * args.split_len;
+    const int p1 = planned ? 0 : min(args.W, p0 + args.split_len);
     // While the previous kernel on the stream may still be running, bring those
     // positions and this head group's q rows into L2. A prefetch returns nothing
     // to the kernel; every load after the wait below sees the previous kernel's
     // writes.
-    {
+    if (!planned) {
         const char* lb = reinterpret_cast<const char*>(args.topk + static_cast<int64_t>(t) * args.W + p0);
         const int lines = (max(0, p1 - p0) * 4 + 127) / 128;
         for (int i = threadIdx.x; i < lines; i += kThreads) prefetch_l2(lb + 128 * i);
@@ -168,11 +217,62 @@ mla_sparse_decode_kernel(const DecodeArgs args) {
     // merge of split partials may then start launching; it waits for this grid.
     pdl_wait();
     pdl_launch_dependents();
+
+    // Planned split: all tokens' list lengths to shared memory (the list area,
+    // free until the piece is copied there); warp 0 finds the chunk length and
+    // this piece's token and entry range, and the first piece of each token
+    // records the token's pieces for the merge. A piece slot past the last piece
+    // has no work and returns.
+    int lbase = 0, n_valid = 0;
+    if (planned) {
+        for (int i = threadIdx.x; i < args.T; i += kThreads) list[i] = __ldg(args.plan_count + i);
+        __syncthreads();
+        if (warp == 0) {
+            const int C = plan_chunk(list, args.T, args.plan_pieces, lane);
+            int acc = 0, tok = -1, first = 0, k_t = 0;
+            for (int base = 0; base < args.T && tok < 0; base += 32) {
+                const int i = base + lane;
+                const int k = (i < args.T) ? max(1, (list[i] + C - 1) / C) : 0;
+                int incl = k;
+#pragma unroll
+                for (int d = 1; d < 32; d <<= 1) {
+                    const int v = __shfl_up_sync(0xffffffffu, incl, d);
+                    if (lane >= d) incl += v;
+                }
+                const unsigned hit = __ballot_sync(0xffffffffu, k > 0 && split >= acc + incl - k && split < acc + incl);
+                if (hit != 0u) {
+                    const int src = __ffs(hit) - 1;
+                    tok = base + src;
+                    first = __shfl_sync(0xffffffffu, acc + incl - k, src);
+                    k_t = __shfl_sync(0xffffffffu, k, src);
+                }
+                acc += __shfl_sync(0xffffffffu, incl, 31);
+            }
+            if (lane == 0) {
+                wcount[0] = tok;
+                if (tok >= 0) {
+                    const int n = list[tok];
+                    const int len = (n + k_t - 1) / k_t;
+                    const int lb = min(n, (split - first) * len);
+                    wcount[1] = lb;
+                    wcount[2] = min(n, lb + len) - lb;
+                    if (split == first && hg == 0) args.plan_tok[tok] = make_int2(first, k_t);
+                }
+            }
+        }
+        __syncthreads();
+        t = wcount[0];
+        if (t < 0) return;
+        lbase = wcount[1];
+        n_valid = wcount[2];
+    }
+
     // The first copy-issuing warp sets up the ring. When this CTA's first 32
     // positions are all present (unsplit or split by positions; through the block
     // table for the paged entry point), they are exactly the first 32 entries of the
     // compacted list, so the warp copies block 0 right away and the copies land
-    // while the whole list is compacted.
+    // while the whole list is compacted. A planned piece holds present slots only:
+    // its first 32 entries are block 0 whenever it has that many.
     bool block0_issued = false;
     if (warp == kProducer) {
         if (lane == 0) {
@@ -184,7 +284,14 @@ mla_sparse_decode_kernel(const DecodeArgs args) {
             fence_mbar_init();
         }
         __syncwarp();
-        if (!by_rank && p1 - p0 >= kNB) {
+        if (planned && n_valid >= kNB) {
+            const int idx = __ldg(args.plan_list + static_cast<int64_t>(t) * args.W + lbase + lane);
+            if (lane == 0) mbar_arrive_expect_tx(&full[0], kNB * kRowRead);
+            __syncwarp();
+            bulk_g2s(stages + lane * kRowBytes, args.cache + static_cast<int64_t>(idx) * args.row_bytes, kRowRead,
+                     &full[0]);
+            block0_issued = true;
+        } else if (!planned && p1 - p0 >= kNB) {
             int idx = __ldg(args.topk + static_cast<int64_t>(t) * args.W + p0 + lane);
             bool present = true;
             if (args.page_size > 0) {
@@ -240,69 +347,55 @@ mla_sparse_decode_kernel(const DecodeArgs args) {
 
     // ---- 1. compact the present entries of this split's positions (all warps) ----
     // Thread i takes a contiguous run of `per` positions, loaded all at once; one
-    // block-wide scan of the per-thread counts places them in position order.
-    const int per = (max(0, p1 - p0) + kThreads - 1) / kThreads;     // <= kPerThread
-    const int32_t* trow = args.topk + static_cast<int64_t>(t) * args.W + p0 + threadIdx.x * per;
-    const int mine = max(0, min(per, p1 - (p0 + static_cast<int>(threadIdx.x) * per)));
-    int idxv[kPerThread];
+    // block-wide scan of the per-thread counts places them in position order. A
+    // planned piece is already compacted: it is copied to the list.
+    if (planned) {
+        const int32_t* src = args.plan_list + static_cast<int64_t>(t) * args.W + lbase;
+        for (int i = threadIdx.x; i < n_valid; i += kThreads) list[i] = __ldg(src + i);
+        lbase = 0;
+        __syncthreads();
+    } else {
+        const int per = (max(0, p1 - p0) + kThreads - 1) / kThreads;     // <= kPerThread
+        const int32_t* trow = args.topk + static_cast<int64_t>(t) * args.W + p0 + threadIdx.x * per;
+        const int mine = max(0, min(per, p1 - (p0 + static_cast<int>(threadIdx.x) * per)));
+        int idxv[kPerThread];
 #pragma unroll
-    for (int k = 0; k < kPerThread; ++k) idxv[k] = (k < mine) ? __ldg(trow + k) : -1;
-    if (args.page_size > 0) {
-        // Positions -> slots (vLLM PR #55277, Purpose item 2): a negative
-        // position or an unassigned (negative) page is absent; a position past
-        // the table is absent and flagged.
-        const int sq = args.token_seq ? __ldg(args.token_seq + t) : 0;
-        const bool seq_ok = sq >= 0 && sq < args.n_seq;
-        const int32_t* bt = args.block_table + static_cast<int64_t>(seq_ok ? sq : 0) * args.bt_pages;
+        for (int k = 0; k < kPerThread; ++k) idxv[k] = (k < mine) ? __ldg(trow + k) : -1;
+        if (args.page_size > 0) {
+            const int sq = args.token_seq ? __ldg(args.token_seq + t) : 0;
+            const bool seq_ok = sq >= 0 && sq < args.n_seq;
+            const int32_t* bt = args.block_table + static_cast<int64_t>(seq_ok ? sq : 0) * args.bt_pages;
+#pragma unroll
+            for (int k = 0; k < kPerThread; ++k) idxv[k] = paged_slot(args, bt, seq_ok, idxv[k]);
+        }
+        int cnt = 0;
 #pragma unroll
         for (int k = 0; k < kPerThread; ++k) {
-            const int pos = idxv[k];
-            if (pos < 0) continue;
-            const int page = pos / args.page_size;
-            if (!seq_ok || page >= args.bt_pages) {
-                atomicOr(args.err, MLA_ERR_DECODE_INDEX_RANGE);
-                idxv[k] = -1;
-                continue;
-            }
-            const int phys = __ldg(bt + page);
-            const int64_t slot = static_cast<int64_t>(phys) * args.page_size + (pos - page * args.page_size);
-            idxv[k] = (phys < 0) ? -1 : static_cast<int>(min(slot, static_cast<int64_t>(INT32_MAX)));
+            const int idx = idxv[k];
+            const bool valid = idx > 0 && static_cast<int64_t>(idx) < args.num_slots;
+            if (idx > 0 && !valid) atomicOr(args.err, MLA_ERR_DECODE_INDEX_RANGE);
+            idxv[k] = valid ? idx : 0;
+            cnt += valid ? 1 : 0;
         }
-    }
-    int cnt = 0;
+        int incl = cnt;
 #pragma unroll
-    for (int k = 0; k < kPerThread; ++k) {
-        const int idx = idxv[k];
-        const bool valid = idx > 0 && static_cast<int64_t>(idx) < args.num_slots;
-        if (idx > 0 && !valid) atomicOr(args.err, MLA_ERR_DECODE_INDEX_RANGE);
-        idxv[k] = valid ? idx : 0;
-        cnt += valid ? 1 : 0;
-    }
-    int incl = cnt;
+        for (int d = 1; d < 32; d <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, d);
+            if (lane >= d) incl += v;
+        }
+        if (lane == 31) wcount[warp] = incl;
+        __syncthreads();
+        int off = incl - cnt;
 #pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-        const int v = __shfl_up_sync(0xffffffffu, incl, d);
-        if (lane >= d) incl += v;
-    }
-    if (lane == 31) wcount[warp] = incl;
-    __syncthreads();
-    int off = incl - cnt, n_valid = 0;
+        for (int w = 0; w < kThreads / 32; ++w) {
+            const int cw = wcount[w];
+            off += (w < warp) ? cw : 0;
+            n_valid += cw;
+        }
 #pragma unroll
-    for (int w = 0; w < kThreads / 32; ++w) {
-        const int cw = wcount[w];
-        off += (w < warp) ? cw : 0;
-        n_valid += cw;
-    }
-#pragma unroll
-    for (int k = 0; k < kPerThread; ++k)
-        if (idxv[k] != 0) list[off++] = idxv[k];
-    __syncthreads();
-    int lbase = 0;     // first list entry of this CTA
-    if (by_rank) {
-        const int shares = min(args.nsplit, max(1, (n_valid + args.rank_chunk - 1) / args.rank_chunk));
-        const int len = (n_valid + shares - 1) / shares;
-        lbase = min(n_valid, split * len);
-        n_valid = min(n_valid, lbase + len) - lbase;
+        for (int k = 0; k < kPerThread; ++k)
+            if (idxv[k] != 0) list[off++] = idxv[k];
+        __syncthreads();
     }
     const int nblk = (n_valid + kNB - 1) / kNB;
 
@@ -659,7 +752,8 @@ mla_sparse_decode_kernel(const DecodeArgs args) {
             }
             if (warp == 0 && c == 0) args.lse[static_cast<int64_t>(t) * H + h] = lse_r[r];
         } else {
-            const int64_t prow = (static_cast<int64_t>(t) * args.nsplit + split) * H + h;
+            const int64_t part = planned ? split : static_cast<int64_t>(t) * args.nsplit + split;
+            const int64_t prow = part * H + h;
             if (warp == 0 && c == 0) args.ws_lse[prow] = lse_r[r];
             if (lt[r] == 0.0f) continue;       // lse = -inf: the merge skips this partial's o
             float* orow = args.ws_o + prow * kLatent + 128 * warp + 32 * c;
@@ -675,27 +769,98 @@ mla_sparse_decode_kernel(const DecodeArgs args) {
     }
 }
 
+// First kernel of a planned split: one CTA per token compacts the present
+// entries of the token's list into plan_list[t][0 .. n_t), in position order,
+// and writes n_t to plan_count[t], with the decode's rules (absent: -1 and other
+// negatives, slot 0, out-of-range slots, which also set the error word; sequence
+// positions mapped through the block table first). Launched with programmatic
+// stream serialization; the decode after it waits for this grid before reading.
+constexpr int kCompactThreads = 256;
+constexpr int kCompactPer = (kListMax + kCompactThreads - 1) / kCompactThreads;
+
+__global__ void __launch_bounds__(kCompactThreads)
+mla_list_compact_kernel(const DecodeArgs args) {
+    __shared__ int wtotal[kCompactThreads / 32];
+    pdl_wait();
+    pdl_launch_dependents();
+    const int t = blockIdx.x;
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int per = (args.W + kCompactThreads - 1) / kCompactThreads;    // <= kCompactPer
+    const int p0 = static_cast<int>(threadIdx.x) * per;
+    const int mine = max(0, min(per, args.W - p0));
+    const int32_t* trow = args.topk + static_cast<int64_t>(t) * args.W + p0;
+    int idxv[kCompactPer];
+#pragma unroll
+    for (int k = 0; k < kCompactPer; ++k) idxv[k] = (k < mine) ? __ldg(trow + k) : -1;
+    if (args.page_size > 0) {
+        const int sq = args.token_seq ? __ldg(args.token_seq + t) : 0;
+        const bool seq_ok = sq >= 0 && sq < args.n_seq;
+        const int32_t* bt = args.block_table + static_cast<int64_t>(seq_ok ? sq : 0) * args.bt_pages;
+#pragma unroll
+        for (int k = 0; k < kCompactPer; ++k) idxv[k] = paged_slot(args, bt, seq_ok, idxv[k]);
+    }
+    int cnt = 0;
+#pragma unroll
+    for (int k = 0; k < kCompactPer; ++k) {
+        const int idx = idxv[k];
+        const bool valid = idx > 0 && static_cast<int64_t>(idx) < args.num_slots;
+        if (idx > 0 && !valid) atomicOr(args.err, MLA_ERR_DECODE_INDEX_RANGE);
+        idxv[k] = valid ? idx : 0;
+        cnt += valid ? 1 : 0;
+    }
+    int incl = cnt;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, d);
+        if (lane >= d) incl += v;
+    }
+    if (lane == 31) wtotal[warp] = incl;
+    __syncthreads();
+    int off = incl - cnt, n = 0;
+#pragma unroll
+    for (int w = 0; w < kCompactThreads / 32; ++w) {
+        off += (w < warp) ? wtotal[w] : 0;
+        n += wtotal[w];
+    }
+    int32_t* dst = args.plan_list + static_cast<int64_t>(t) * args.W;
+#pragma unroll
+    for (int k = 0; k < kCompactPer; ++k)
+        if (idxv[k] != 0) dst[off++] = idxv[k];
+    if (threadIdx.x == 0) args.plan_count[t] = n;
+}
+
 // Merge of the split partials of one (token, head): lse = ln sum_s exp(lse_s),
 // out = sum_s exp(lse_s - lse) o_s, in split order; a NaN partial makes both NaN. Thread x takes dims 4x ..
 // 4x + 3; the loads of kMergeBatch splits are issued together. Launched with
 // programmatic stream serialization behind the decode, whose grid it waits for.
+// The partials of token t are rows t * nsplit .. t * nsplit + nsplit - 1, or,
+// after a planned split, the token's pieces as the decode recorded them.
 constexpr int kMergeBatch = 8;
 
 __global__ void __launch_bounds__(128)
 mla_split_combine_kernel(const float* __restrict__ ws_o, const float* __restrict__ ws_lse,
-                         int H, int nsplit, __nv_bfloat16* __restrict__ out, float* __restrict__ lse) {
+                         const int2* __restrict__ plan_tok, int plan_pieces, int H, int nsplit,
+                         __nv_bfloat16* __restrict__ out, float* __restrict__ lse) {
     pdl_wait();
     const int64_t th = blockIdx.x;              // t * H + h
     const int64_t t = th / H;
     const int h = static_cast<int>(th % H);
     const int d = 4 * threadIdx.x;
+    int64_t row0 = t * nsplit;                  // first partial of the token
+    int np = nsplit;                            // its number of partials
+    if (plan_tok != nullptr) {
+        const int2 pt = plan_tok[t];
+        row0 = min(max(pt.x, 0), plan_pieces - 1);
+        np = min(max(pt.y, 1), plan_pieces - static_cast<int>(row0));
+    }
     float mx = -INFINITY;
     bool nan = false;
-    for (int s0 = 0; s0 < nsplit; s0 += kMergeBatch) {
+    for (int s0 = 0; s0 < np; s0 += kMergeBatch) {
         float ls[kMergeBatch];
 #pragma unroll
         for (int q = 0; q < kMergeBatch; ++q)
-            ls[q] = (s0 + q < nsplit) ? ws_lse[(t * nsplit + s0 + q) * H + h] : -INFINITY;
+            ls[q] = (s0 + q < np) ? ws_lse[(row0 + s0 + q) * H + h] : -INFINITY;
 #pragma unroll
         for (int q = 0; q < kMergeBatch; ++q) {
             mx = fmaxf(mx, ls[q]);
@@ -717,13 +882,13 @@ mla_split_combine_kernel(const float* __restrict__ ws_o, const float* __restrict
     }
     float wsum = 0.0f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int s0 = 0; s0 < nsplit; s0 += kMergeBatch) {
+    for (int s0 = 0; s0 < np; s0 += kMergeBatch) {
         float ls[kMergeBatch];
         float4 v[kMergeBatch];
 #pragma unroll
         for (int q = 0; q < kMergeBatch; ++q) {
-            const int64_t prow = (t * nsplit + min(s0 + q, nsplit - 1)) * H + h;
-            ls[q] = (s0 + q < nsplit) ? ws_lse[prow] : -INFINITY;
+            const int64_t prow = (row0 + min(s0 + q, np - 1)) * H + h;
+            ls[q] = (s0 + q < np) ? ws_lse[prow] : -INFINITY;
             // A split with no present entry (lse -inf) left its o unwritten.
             v[q] = (ls[q] == -INFINITY) ? make_float4(0.f, 0.f, 0.f, 0.f)
                                         : *reinterpret_cast<const float4*>(ws_o + prow * kLatent + d);
@@ -769,21 +934,41 @@ int choose_nsplit(int T, int H, int W, int sms) {
     return static_cast<int>(ns);
 }
 
-// Lists that one CTA can compact are split by present entries, so that a list
-// whose entries are all in its first positions (a short sequence in a wide
-// buffer) still spreads over as many CTAs as it has rows for: a list of c
-// present entries takes ceil(c / rank_chunk) CTAs, and the CTAs left over exit
-// after the compaction. Longer lists are split by positions.
-int rank_chunk_for(int W, int nsplit) {
-    if (nsplit <= 1 || W > kListMax) return 0;
-    return (W + nsplit - 1) / nsplit;
+// Lists that one CTA can compact are split by a plan (see the kernel's header):
+// `pieces` piece slots per head group, one wave of CTAs at kSplitCtasPerSm per SM
+// and never fewer than the tokens (T * head_groups < SMs whenever a list is
+// split, so this bound is slack). Longer lists are split by positions (pieces 0).
+struct Split {
+    int nsplit;
+    int pieces;
+};
+
+Split choose_split(int T, int H, int W, int sms) {
+    Split sp{choose_nsplit(T, H, W, sms), 0};
+    if (sp.nsplit > 1 && W <= kListMax && T <= kListMax) {
+        const int head_groups = (H + kHeads - 1) / kHeads;
+        sp.pieces = max(T, kSplitCtasPerSm * sms / head_groups);
+    }
+    return sp;
 }
 
-size_t workspace_for(int T, int H, int nsplit) {
-    if (nsplit <= 1) return 0;
-    const size_t rows = static_cast<size_t>(T) * nsplit * H;
-    const size_t o_bytes = rows * kLatent * sizeof(float);
-    return o_bytes + ((rows * sizeof(float) + 255) & ~static_cast<size_t>(255));
+size_t align256(size_t n) { return (n + 255) & ~static_cast<size_t>(255); }
+
+// Rows of split partials: T * nsplit * H, or pieces * H when planned.
+size_t partial_rows(int T, int H, const Split& sp) {
+    return sp.pieces > 0 ? static_cast<size_t>(sp.pieces) * H : static_cast<size_t>(T) * sp.nsplit * H;
+}
+
+// Workspace: the partial o rows, their lse, and for a planned split the
+// compacted lists [T, W], their lengths [T] and each token's pieces [T].
+size_t workspace_for(int T, int H, int W, const Split& sp) {
+    if (sp.nsplit <= 1) return 0;
+    const size_t rows = partial_rows(T, H, sp);
+    size_t bytes = rows * kLatent * sizeof(float) + align256(rows * sizeof(float));
+    if (sp.pieces > 0)
+        bytes += align256(static_cast<size_t>(T) * W * sizeof(int32_t)) + align256(static_cast<size_t>(T) * sizeof(int32_t)) +
+                 align256(static_cast<size_t>(T) * sizeof(int2));
+    return bytes;
 }
 
 }  // namespace
@@ -792,7 +977,7 @@ extern "C" size_t mla_sparse_decode_workspace_bytes(int T, int H, int W) {
     if (T <= 0 || H <= 0 || H > 128 || W < 0) return 0;
     const int sms = mla_host::sm_count();
     if (sms <= 0) return 0;
-    return workspace_for(T, H, choose_nsplit(T, H, W, sms));
+    return workspace_for(T, H, W, choose_split(T, H, W, sms));
 }
 
 namespace {
@@ -821,13 +1006,17 @@ int launch_decode(const void* q_bf16, int T, int H, int d_qk, mla_kv_cache_t kv,
     int* err = mla_host::device_error_word();
     const int sms = mla_host::sm_count();
     if (err == nullptr || sms <= 0) return MLA_ECUDA;
-    const int nsplit = choose_nsplit(T, H, W, sms);
-    const size_t need = workspace_for(T, H, nsplit);
+    const Split sp = choose_split(T, H, W, sms);
+    const int nsplit = sp.nsplit;
+    const bool planned = sp.pieces > 0;
+    const size_t need = workspace_for(T, H, W, sp);
     if (need > 0 && (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)))
         return MLA_ENOWORKSPACE;
 
-    if (!mla_host::max_dynamic_smem(reinterpret_cast<const void*>(mla_sparse_decode_kernel<true>), kSmemTotal) ||
-        !mla_host::max_dynamic_smem(reinterpret_cast<const void*>(mla_sparse_decode_kernel<false>), kSmemTotal))
+    if (!mla_host::max_dynamic_smem(reinterpret_cast<const void*>(mla_sparse_decode_kernel<true, false>), kSmemTotal) ||
+        !mla_host::max_dynamic_smem(reinterpret_cast<const void*>(mla_sparse_decode_kernel<false, false>), kSmemTotal) ||
+        !mla_host::max_dynamic_smem(reinterpret_cast<const void*>(mla_sparse_decode_kernel<true, true>), kSmemTotal) ||
+        !mla_host::max_dynamic_smem(reinterpret_cast<const void*>(mla_sparse_decode_kernel<false, true>), kSmemTotal))
         return MLA_ECUDA;
     DecodeArgs a;
     a.q = static_cast<const __nv_bfloat16*>(q_bf16);
@@ -835,10 +1024,23 @@ int launch_decode(const void* q_bf16, int T, int H, int d_qk, mla_kv_cache_t kv,
     a.topk = topk_idx;
     a.out = static_cast<__nv_bfloat16*>(out_bf16);
     a.lse = lse;
+    const size_t rows = partial_rows(T, H, sp);
     a.ws_o = static_cast<float*>(workspace);
-    a.ws_lse = nsplit > 1 ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
-                                                     static_cast<size_t>(T) * nsplit * H * kLatent * sizeof(float))
+    a.ws_lse = nsplit > 1 ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + rows * kLatent * sizeof(float))
                           : nullptr;
+    a.plan_list = nullptr;
+    a.plan_count = nullptr;
+    a.plan_tok = nullptr;
+    a.plan_pieces = 0;
+    if (planned) {
+        uint8_t* p = reinterpret_cast<uint8_t*>(a.ws_lse) + align256(rows * sizeof(float));
+        a.plan_list = reinterpret_cast<int32_t*>(p);
+        p += align256(static_cast<size_t>(T) * W * sizeof(int32_t));
+        a.plan_count = reinterpret_cast<int32_t*>(p);
+        p += align256(static_cast<size_t>(T) * sizeof(int32_t));
+        a.plan_tok = reinterpret_cast<int2*>(p);
+        a.plan_pieces = sp.pieces;
+    }
     a.err = err;
     a.num_slots = kv.num_slots;
     a.row_bytes = kv.row_bytes;
@@ -849,22 +1051,37 @@ int launch_decode(const void* q_bf16, int T, int H, int d_qk, mla_kv_cache_t kv,
     a.page_size = pg.page_size;
     a.T = T; a.H = H; a.d_qk = d_qk; a.W = W; a.nsplit = nsplit;
     a.split_len = (W + nsplit - 1) / nsplit;
-    a.rank_chunk = rank_chunk_for(W, nsplit);
     a.sm_scale_log2 = sm_scale * kLog2e;
-    const dim3 grid(static_cast<unsigned>(static_cast<int64_t>(T) * ((H + kHeads - 1) / kHeads)), static_cast<unsigned>(nsplit));
+    const int head_groups = (H + kHeads - 1) / kHeads;
+    const dim3 grid = planned ? dim3(static_cast<unsigned>(sp.pieces * head_groups), 1u)
+                              : dim3(static_cast<unsigned>(static_cast<int64_t>(T) * head_groups), static_cast<unsigned>(nsplit));
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    if (planned) {
+        cudaLaunchConfig_t ccfg = {};
+        ccfg.gridDim = dim3(static_cast<unsigned>(T));
+        ccfg.blockDim = dim3(kCompactThreads);
+        ccfg.stream = st;
+        ccfg.attrs = attr;
+        ccfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&ccfg, mla_list_compact_kernel, a) != cudaSuccess || cudaGetLastError() != cudaSuccess)
+            return MLA_ECUDA;
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = kSmemTotal;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    const cudaError_t lr = (d_qk == kLatent + kRope) ? cudaLaunchKernelEx(&cfg, mla_sparse_decode_kernel<true>, a)
-                                                     : cudaLaunchKernelEx(&cfg, mla_sparse_decode_kernel<false>, a);
+    const bool rope = d_qk == kLatent + kRope;
+    const cudaError_t lr =
+        planned ? (rope ? cudaLaunchKernelEx(&cfg, mla_sparse_decode_kernel<true, true>, a)
+                        : cudaLaunchKernelEx(&cfg, mla_sparse_decode_kernel<false, true>, a))
+                : (rope ? cudaLaunchKernelEx(&cfg, mla_sparse_decode_kernel<true, false>, a)
+                        : cudaLaunchKernelEx(&cfg, mla_sparse_decode_kernel<false, false>, a));
     if (lr != cudaSuccess || cudaGetLastError() != cudaSuccess) return MLA_ECUDA;
     if (nsplit > 1) {
         cudaLaunchConfig_t mcfg = {};
@@ -874,7 +1091,8 @@ int launch_decode(const void* q_bf16, int T, int H, int d_qk, mla_kv_cache_t kv,
         mcfg.attrs = attr;
         mcfg.numAttrs = 1;
         if (cudaLaunchKernelEx(&mcfg, mla_split_combine_kernel, static_cast<const float*>(a.ws_o),
-                               static_cast<const float*>(a.ws_lse), H, nsplit, a.out, a.lse) != cudaSuccess ||
+                               static_cast<const float*>(a.ws_lse), static_cast<const int2*>(a.plan_tok), a.plan_pieces,
+                               H, nsplit, a.out, a.lse) != cudaSuccess ||
             cudaGetLastError() != cudaSuccess)
             return MLA_ECUDA;
     }

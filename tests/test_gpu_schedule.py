@@ -1,8 +1,10 @@
 """The decode's work split against the float64 oracle.
 
-With fewer (token, head group) units than the GPU has SMs, each token's list is
-split across CTAs by present entries and the partials merged; with more units,
-one CTA takes one unit whole. The lists here are built to reach the corners of
+With fewer (token, head group) units than the GPU has SMs, a first kernel
+compacts each token's list, the decode cuts every list into pieces of at most C
+present entries (C chosen so that all pieces fit in one wave of CTAs, so a long
+list gets more pieces than a short one) and a third kernel merges each token's
+partials; with more units, one CTA takes one unit whole. The lists here are built to reach the corners of
 both: tokens with no present entry, one entry, 31 / 32 / 33 entries (a block
 boundary), full lists, present entries scattered among -1 or packed at the
 front, and head counts that leave a short last head group.
@@ -82,6 +84,53 @@ def test_split_lists_with_a_short_last_head_group():
 
 def test_split_lists_nope_rows():
     _run([900, 450, 1, 0, 64, 899, 300], 16, 900, seed=23, d_qk=512)
+
+
+def test_planned_split_one_long_list_among_short_ones():
+    # One full 2,304-entry list among 32 one-entry lists: the long list is cut into
+    # many pieces (more than one merge batch of partials), the short ones into one.
+    out = _run([2304] + [1] * 32, 16, 2304, seed=26)
+    # The same call again is bit-identical (the plan and the merge order are fixed).
+    q, gc, topk, sm, o1, l1 = out
+    o2, l2 = M.mla_sparse_decode(q.to(dev()), gc, topk.to(dev()), sm)
+    torch.cuda.synchronize()
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
+    assert torch.equal(l1.view(torch.int32), l2.view(torch.int32))
+
+
+def test_planned_split_near_the_sm_count_sampled():
+    # 150 tokens (just under one unit per SM) with lists up to 2,304 entries: the
+    # pieces just fit in one wave; compared on a sample of tokens.
+    rng = np.random.default_rng(27)
+    counts = rng.integers(0, 2305, size=150).tolist()
+    counts[:4] = [2304, 0, 2304, 1]
+    tokens = sorted(set(rng.choice(150, 12, replace=False).tolist()) | {0, 1, 2, 3, 149})
+    _run(counts, 16, 2304, seed=27, tokens=tokens)
+
+
+def test_planned_split_paged_with_holes_and_range():
+    # The planned split through the block table: 6 tokens of 1,024 positions over
+    # 3 sequences, unassigned pages and positions past the table (absent and flagged).
+    gc, cc = _cache(28)
+    rng = np.random.default_rng(28)
+    T, H, W, page, n_seq, max_pages = 6, 16, 1024, 16, 3, 200
+    bt = rng.permutation(np.arange(1, NUM_SLOTS // page))[: n_seq * max_pages].astype(np.int32).reshape(n_seq, max_pages)
+    bt[rng.random(bt.shape) < 0.1] = -1
+    pos = np.stack([rng.permutation(max_pages * page + 64)[:W] for _ in range(T)]).astype(np.int32)
+    pos[rng.random(pos.shape) < 0.2] = -1
+    pos[4, :] = -1                                          # an empty list
+    seq = rng.integers(0, n_seq, size=T).astype(np.int32)
+    q = torch.from_numpy(rng.standard_normal((T, H, 576)).astype(np.float32)).to(torch.bfloat16)
+    assert M.mla_sparse_decode_workspace_bytes(T, H, W) > 0, "this case is meant to split"
+    M.mla_get_error()
+    out, lse = M.mla_sparse_decode_paged(q.to(dev()), gc, torch.from_numpy(pos).to(dev()),
+                                         torch.from_numpy(bt).to(dev()), page, 0.05,
+                                         token_seq=torch.from_numpy(seq).to(dev()))
+    torch.cuda.synchronize()
+    phys, bad = oracle.paged_to_physical(pos, bt, page, seq)
+    assert bad > 0 and M.mla_get_error() == M.MLA_ERR_DECODE_INDEX_RANGE
+    ro, rl, _ = oracle.sparse_decode(q, cc, phys, 0.05)
+    check_decode(out, lse, ro, rl)
 
 
 def test_many_units_random_counts_sampled():
