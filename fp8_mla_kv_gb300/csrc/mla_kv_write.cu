@@ -8,7 +8,8 @@
 // Rows are 656 bytes, or 528 for the canonical NoPE row without a tail
 // (sglang PR #39288, "Relation to other changes": flashinfer#5075).
 //
-// One warp per row. Lane l owns latent values 16l .. 16l+15 (two 16-byte
+// One warp per row, or two rows per warp at a time on large batches (both rows'
+// loads in flight together). Lane l owns latent values 16l .. 16l+15 (two 16-byte
 // loads), so tile t = lanes 8t .. 8t+7 and the tile amax is a 3-step xor
 // shuffle. The 512 FP8 bytes leave in one fully coalesced 16-byte store per
 // lane; lanes 0..7 then store the 128-byte tail and lane 8 the 16 bytes of
@@ -20,7 +21,7 @@ namespace {
 
 using namespace mla;
 
-constexpr int kWriterThreads = 256;   // 8 rows in flight per CTA
+constexpr int kWriterThreads = 256;   // 8 or 16 rows in flight per CTA
 
 __device__ __forceinline__ uint64_t f32x2(float lo, float hi) {
     uint64_t r;
@@ -52,7 +53,91 @@ __device__ __forceinline__ uint32_t quant2_ieee(float x0, float x1, float scale)
     return static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(v, __NV_SATFINITE, __NV_E4M3));
 }
 
-__global__ void __launch_bounds__(kWriterThreads, 8)
+// Inputs of one row in flight: lane l's 32 latent bytes and, for lanes 0..7, 16
+// bytes of the RoPE tail.
+struct RowIn {
+    uint4 a, b, tail;
+};
+
+__device__ __forceinline__ RowIn load_row(const uint16_t* __restrict__ latent, const uint16_t* __restrict__ rope,
+                                          int64_t r, int lane) {
+    RowIn in;
+    const uint8_t* src = reinterpret_cast<const uint8_t*>(latent + r * kLatent) + 32 * lane;
+    in.a = ld_nc_v4(src);
+    in.b = ld_nc_v4(src + 16);
+    in.tail = make_uint4(0u, 0u, 0u, 0u);
+    if (rope != nullptr && lane < 8)
+        in.tail = ld_nc_v4(reinterpret_cast<const uint8_t*>(rope + r * kRope) + 16 * lane);
+    return in;
+}
+
+// Tile amax, scale, E4M3 codes and the row's stores (the whole warp).
+__device__ __forceinline__ void quantise_store(const RowIn& in, uint8_t* row, int64_t row_bytes, int lane) {
+    const uint32_t w[8] = {in.a.x, in.a.y, in.a.z, in.a.w, in.b.x, in.b.y, in.b.z, in.b.w};
+    float v[16];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        v[2 * i] = bf16lo(w[i]);
+        v[2 * i + 1] = bf16hi(w[i]);
+    }
+    float amax = 0.0f;                                   // fmaxf ignores NaN
+#pragma unroll
+    for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
+    const float scale = (amax > 0.0f) ? __fdiv_rn(amax, MLA_FP8_MAX) : 1.0f;
+    const bool fast = scale >= kDivFastMin && scale <= kDivFastMax;   // false only for extreme tiles
+    const float rcp = __frcp_rn(scale);
+
+    // One branch for the whole warp: every tile of the row in the fast range
+    // (the rule), or the IEEE division on the tiles that are not.
+    uint32_t qv[4];
+    if (__all_sync(0xffffffffu, fast)) {
+        const uint64_t y2 = f32x2(rcp, rcp), ns2 = f32x2(-scale, -scale);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            qv[k] = quant2_fast(v[4 * k], v[4 * k + 1], y2, ns2) |
+                    (quant2_fast(v[4 * k + 2], v[4 * k + 3], y2, ns2) << 16);
+    } else {
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            qv[k] = fast ? (static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(
+                                make_float2(div_by_scale(v[4 * k], scale, rcp), div_by_scale(v[4 * k + 1], scale, rcp)),
+                                __NV_SATFINITE, __NV_E4M3)) |
+                            (static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(
+                                make_float2(div_by_scale(v[4 * k + 2], scale, rcp), div_by_scale(v[4 * k + 3], scale, rcp)),
+                                __NV_SATFINITE, __NV_E4M3)) << 16))
+                         : (quant2_ieee(v[4 * k], v[4 * k + 1], scale) |
+                            (quant2_ieee(v[4 * k + 2], v[4 * k + 3], scale) << 16));
+    }
+
+    st_v4(row + 16 * lane, make_uint4(qv[0], qv[1], qv[2], qv[3]));
+    const float s0 = __shfl_sync(0xffffffffu, scale, 0);
+    const float s1 = __shfl_sync(0xffffffffu, scale, 8);
+    const float s2 = __shfl_sync(0xffffffffu, scale, 16);
+    const float s3 = __shfl_sync(0xffffffffu, scale, 24);
+    if (lane < 8) {
+        if (row_bytes == kRowBytes) st_v4(row + kTailOff + 16 * lane, in.tail);
+    } else if (lane == 8) {
+        st_v4(row + kScaleOff, make_uint4(__float_as_uint(s0), __float_as_uint(s1),
+                                          __float_as_uint(s2), __float_as_uint(s3)));
+    }
+}
+
+// Whether a row with this slot is written; an out-of-range slot sets the error
+// word (lane 0) and is dropped like the reserved slot and negative slots.
+__device__ __forceinline__ bool keep_slot(int64_t slot, int64_t num_slots, int64_t reserved_slot, int* err,
+                                          int lane) {
+    if (slot == reserved_slot || slot < 0) return false;
+    if (slot >= num_slots) {
+        if (lane == 0) atomicOr(err, MLA_ERR_WRITE_SLOT_RANGE);
+        return false;
+    }
+    return true;
+}
+
+__global__ void __launch_bounds__(kWriterThreads, 4)
 mla_kv_write_kernel(uint8_t* __restrict__ cache, int64_t num_slots, int64_t row_bytes,
                     const int64_t* __restrict__ slot_idx,
                     const uint16_t* __restrict__ latent,
@@ -66,73 +151,21 @@ mla_kv_write_kernel(uint8_t* __restrict__ cache, int64_t num_slots, int64_t row_
     pdl_wait();
     pdl_launch_dependents();
     const int lane = threadIdx.x & 31;
-    const int64_t stride = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
-    for (int64_t r = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; r < n_rows;
-         r += stride) {
-        const int64_t slot = __ldg(slot_idx + r);            // same for the whole warp
-        if (slot == reserved_slot || slot < 0) continue;     // dropped: no input is read
-        if (slot >= num_slots) {
-            if (lane == 0) atomicOr(err, MLA_ERR_WRITE_SLOT_RANGE);
-            continue;
-        }
-        const uint8_t* src = reinterpret_cast<const uint8_t*>(latent + r * kLatent) + 32 * lane;
-        const uint4 a = ld_nc_v4(src);
-        const uint4 b = ld_nc_v4(src + 16);
-        uint4 tail = make_uint4(0u, 0u, 0u, 0u);
-        if (rope != nullptr && lane < 8)
-            tail = ld_nc_v4(reinterpret_cast<const uint8_t*>(rope + r * kRope) + 16 * lane);
-
-        const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-        float v[16];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            v[2 * i] = bf16lo(w[i]);
-            v[2 * i + 1] = bf16hi(w[i]);
-        }
-        float amax = 0.0f;                                   // fmaxf ignores NaN
-#pragma unroll
-        for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
-        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
-        const float scale = (amax > 0.0f) ? __fdiv_rn(amax, MLA_FP8_MAX) : 1.0f;
-        const bool fast = scale >= kDivFastMin && scale <= kDivFastMax;   // false only for extreme tiles
-        const float rcp = __frcp_rn(scale);
-
-        // One branch for the whole warp: every tile of the row in the fast range
-        // (the rule), or the IEEE division on the tiles that are not.
-        uint32_t qv[4];
-        if (__all_sync(0xffffffffu, fast)) {
-            const uint64_t y2 = f32x2(rcp, rcp), ns2 = f32x2(-scale, -scale);
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-                qv[k] = quant2_fast(v[4 * k], v[4 * k + 1], y2, ns2) |
-                        (quant2_fast(v[4 * k + 2], v[4 * k + 3], y2, ns2) << 16);
-        } else {
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-                qv[k] = fast ? (static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(
-                                    make_float2(div_by_scale(v[4 * k], scale, rcp), div_by_scale(v[4 * k + 1], scale, rcp)),
-                                    __NV_SATFINITE, __NV_E4M3)) |
-                                (static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(
-                                    make_float2(div_by_scale(v[4 * k + 2], scale, rcp), div_by_scale(v[4 * k + 3], scale, rcp)),
-                                    __NV_SATFINITE, __NV_E4M3)) << 16))
-                             : (quant2_ieee(v[4 * k], v[4 * k + 1], scale) |
-                                (quant2_ieee(v[4 * k + 2], v[4 * k + 3], scale) << 16));
-        }
-
-        uint8_t* row = cache + slot * row_bytes;
-        st_v4(row + 16 * lane, make_uint4(qv[0], qv[1], qv[2], qv[3]));
-        const float s0 = __shfl_sync(0xffffffffu, scale, 0);
-        const float s1 = __shfl_sync(0xffffffffu, scale, 8);
-        const float s2 = __shfl_sync(0xffffffffu, scale, 16);
-        const float s3 = __shfl_sync(0xffffffffu, scale, 24);
-        if (lane < 8) {
-            if (row_bytes == kRowBytes) st_v4(row + kTailOff + 16 * lane, tail);
-        } else if (lane == 8) {
-            st_v4(row + kScaleOff, make_uint4(__float_as_uint(s0), __float_as_uint(s1),
-                                              __float_as_uint(s2), __float_as_uint(s3)));
-        }
+    const int64_t nw = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;   // warps in the grid
+    // Warp w takes rows w and w + nw of each group of 2 * nw rows: both slots, then
+    // both rows' inputs are loaded before either is quantised.
+    for (int64_t ra = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; ra < n_rows;
+         ra += 2 * nw) {
+        const int64_t rb = ra + nw;
+        const int64_t sa = __ldg(slot_idx + ra);             // same for the whole warp
+        const int64_t sb = (rb < n_rows) ? __ldg(slot_idx + rb) : -1;
+        const bool ka = keep_slot(sa, num_slots, reserved_slot, err, lane);   // dropped: no input is read
+        const bool kb = keep_slot(sb, num_slots, reserved_slot, err, lane);
+        RowIn ia, ib;
+        if (ka) ia = load_row(latent, rope, ra, lane);
+        if (kb) ib = load_row(latent, rope, rb, lane);
+        if (ka) quantise_store(ia, cache + sa * row_bytes, row_bytes, lane);
+        if (kb) quantise_store(ib, cache + sb * row_bytes, row_bytes, lane);
     }
 }
 
@@ -153,9 +186,16 @@ extern "C" int mla_kv_write(mla_kv_cache_t kv, const int64_t* slot_idx, const vo
     int* err = mla_host::device_error_word();
     const int sms = mla_host::sm_count();
     if (err == nullptr || sms <= 0) return MLA_ECUDA;
-    const int64_t rows_per_cta = kWriterThreads / 32;
-    int64_t blocks = (n_rows + rows_per_cta - 1) / rows_per_cta;
-    const int64_t max_blocks = static_cast<int64_t>(sms) * 8;     // 64 resident warps per SM
+    // One row per warp while that takes at most two CTAs per SM (a small batch is
+    // done soonest by the most warps); above that two rows per warp, both rows'
+    // loads in flight together, and at most four CTAs per SM (32 warps) with the
+    // grid striding over larger batches. Measured with 100 calls per graph: 8,192
+    // rows 4.0 us per call against 5.4 at one row per warp on up to eight CTAs
+    // per SM; 1,048,575 rows 0.85 of the HBM copy rate against 0.75.
+    const int64_t warps_per_cta = kWriterThreads / 32;
+    int64_t blocks = (n_rows + warps_per_cta - 1) / warps_per_cta;
+    if (blocks > 2 * static_cast<int64_t>(sms)) blocks = (n_rows + 2 * warps_per_cta - 1) / (2 * warps_per_cta);
+    const int64_t max_blocks = static_cast<int64_t>(sms) * 4;
     if (blocks > max_blocks) blocks = max_blocks;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(blocks));

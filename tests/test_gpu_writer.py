@@ -84,3 +84,29 @@ def test_empty_and_invalid_calls():
         M.mla_kv_write(g, torch.ones(2, dtype=torch.int64, device=d), lat, None)
     torch.cuda.synchronize()
     assert torch.all(g == 0)
+
+
+@pytest.mark.parametrize("n_rows", [2432, 2433, 2440, 5001, 40000])
+def test_batches_around_two_rows_per_warp(n_rows):
+    # Large batches run two rows per warp (both rows' loads in flight together) and,
+    # past four CTAs per SM, stride over the batch. Batch sizes on both sides of the
+    # switch and with a ragged last group, a quarter of the rows aimed at the
+    # reserved slot, a few out of range (dropped and flagged), RoPE and NoPE rows:
+    # every byte of the cache as the oracle writes it.
+    gen = torch.Generator().manual_seed(n_rows)
+    num_slots = 2 * n_rows + 16
+    slots = (torch.randperm(num_slots - 1, generator=gen)[:n_rows] + 1).to(torch.int64)
+    slots[torch.randperm(n_rows, generator=gen)[: n_rows // 4]] = 0
+    slots[torch.randperm(n_rows, generator=gen)[:3]] = num_slots + 5
+    lat = (torch.randn((n_rows, 512), generator=gen) * 3.0).to(torch.bfloat16)
+    rope = torch.randn((n_rows, 64), generator=gen).to(torch.bfloat16)
+    for rp in (rope, None):
+        wb = workloads.WriteBatch(slots, lat, rp)
+        wl = workloads.Workload("writer-batch", num_slots, 0, None, [wb], None)
+        M.mla_get_error()
+        g, c = gpu_cache(wl), cpu_cache(wl)
+        gpu_write(g, wb)
+        cpu_write(c, wb)
+        torch.cuda.synchronize()
+        assert M.mla_get_error() == M.MLA_ERR_WRITE_SLOT_RANGE
+        assert np.array_equal(g.cpu().numpy(), c)
