@@ -15,6 +15,8 @@
 // stores) and lanes 0..7 store the 128-byte tail (pe_dim 64) or zeros (pe_dim 0:
 // the tail is not read). An absent slot (<= 0) gives a row of zeros; a slot >=
 // num_slots also sets MLA_ERR_GATHER_INDEX_RANGE.
+#include <cfloat>
+
 #include "mla_device.cuh"
 
 namespace {
@@ -65,16 +67,29 @@ constexpr int kUCtasPerSm = 2;
 // warp w widens rows w, w + 12, w + 24 of the block from shared memory.
 // Two products rounded to BF16 by the hardware conversion (round to nearest even
 // of the fp32 product). That is the nearest BF16 of the exact product unless the
-// fp32 product sits on a BF16 midpoint, is NaN, or is nonzero below 2^-100; such
-// values raise `exact` and are redone by product_to_bf16.
+// fp32 product sits on a BF16 midpoint, is NaN, or is nonzero below 2^-100. The
+// last two are ruled out per row (row_needs_exact); a midpoint raises `exact`, and
+// such rows are redone by product_to_bf16.
 __device__ __forceinline__ uint32_t pair_to_bf16x2(float v0, float v1, float s, bool& exact) {
     const float p0 = __fmul_rn(v0, s), p1 = __fmul_rn(v1, s);
     const uint32_t u0 = __float_as_uint(p0), u1 = __float_as_uint(p1);
-    exact |= ((u0 & 0xFFFFu) == 0x8000u) | ((u1 & 0xFFFFu) == 0x8000u) |
-             ((p0 != 0.0f) & !(fabsf(p0) >= 0x1p-100f)) | ((p1 != 0.0f) & !(fabsf(p1) >= 0x1p-100f));
+    exact |= ((u0 & 0xFFFFu) == 0x8000u) | ((u1 & 0xFFFFu) == 0x8000u);
     uint32_t r;
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(p1), "f"(p0));   // high half <- p1
     return r;
+}
+
+// Whether a lane's 16 codes with tile scale s can give a product that the
+// hardware conversion does not round as required: s outside [2^-80, FLT_MAX]
+// (NaN, infinite, negative, zero or tiny: with s >= 2^-80 a nonzero E4M3 value,
+// at least 2^-9 in magnitude, gives a product of at least 2^-89), or a NaN code
+// (S.1111.111: the low seven bits of a byte all set).
+__device__ __forceinline__ bool row_needs_exact(const uint4& codes, float s) {
+    const uint32_t w[4] = {codes.x, codes.y, codes.z, codes.w};
+    uint32_t nan = 0u;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) nan |= ((w[q] & 0x7F7F7F7Fu) + 0x01010101u) & 0x80808080u;
+    return nan != 0u || !(s >= 0x1p-80f && s <= FLT_MAX);
 }
 
 __global__ void __launch_bounds__(kUThreads, kUCtasPerSm)
@@ -172,7 +187,7 @@ mla_gather_upconvert_kernel(const uint8_t* __restrict__ cache, int64_t num_slots
                 v[4 * q + 3] = __half2float(__ushort_as_half(static_cast<unsigned short>(h23 >> 16)));
             }
             uint32_t o[8];
-            bool exact = false;
+            bool exact = row_needs_exact(codes, sc);
 #pragma unroll
             for (int q = 0; q < 8; ++q) o[q] = pair_to_bf16x2(v[2 * q], v[2 * q + 1], sc, exact);
             if (exact) {                                              // rare
