@@ -130,9 +130,10 @@ size_t mla_sparse_decode_workspace_bytes(int T, int H, int W);
 /*
  * mla_sparse_decode - sparse top-k MLA decode over the packed FP8 cache.
  *
- * Defined by the benchmark spec of the decode together with sglang PR #47013
- * (Motivation: unused top-k entries must not reach the result, even when slot 0
- * holds NaN), sglang PR #39288 ("SM120 sparse MLA: zero-initialise the
+ * Sparse top-k MLA attention over the listed rows, written out below, with the
+ * masking rules of sglang PR #47013 (Motivation: unused top-k entries must not
+ * reach the result, even when slot 0 holds NaN), sglang PR #39288 ("SM120
+ * sparse MLA: zero-initialise the
  * page-split scratch", Root cause: a -1 candidate contributes nothing and must
  * not gather slot 0), and vLLM PR #55277 (Purpose item 2: the index buffer
  * width W is a capacity; the active entries are bounded by the -1 padding;
