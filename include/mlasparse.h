@@ -133,9 +133,8 @@ size_t mla_sparse_decode_workspace_bytes(int T, int H, int W);
  * Sparse top-k MLA attention over the listed rows, written out below, with the
  * masking rules of sglang PR #47013 (Motivation: unused top-k entries must not
  * reach the result, even when slot 0 holds NaN), sglang PR #39288 ("SM120
- * sparse MLA: zero-initialise the
- * page-split scratch", Root cause: a -1 candidate contributes nothing and must
- * not gather slot 0), and vLLM PR #55277 (Purpose item 2: the index buffer
+ * sparse MLA: zero-initialise the page-split scratch", Root cause: a -1
+ * candidate contributes nothing and must not gather slot 0), and vLLM PR #55277 (Purpose item 2: the index buffer
  * width W is a capacity; the active entries are bounded by the -1 padding;
  * Purpose item 1 and "Relation to #53969": NoPE decode reads no tail).
  *
