@@ -21,7 +21,8 @@ namespace {
 
 using namespace mla;
 
-constexpr int kWriterThreads = 256;   // 8 or 16 rows in flight per CTA
+constexpr int kWriterThreads = 64;    // 2 warps: 2 or 4 rows in flight per CTA
+constexpr int kWriterWarpsPerSm = 32; // at most half of an SM's warp slots
 
 __device__ __forceinline__ uint64_t f32x2(float lo, float hi) {
     uint64_t r;
@@ -137,7 +138,7 @@ __device__ __forceinline__ bool keep_slot(int64_t slot, int64_t num_slots, int64
     return true;
 }
 
-__global__ void __launch_bounds__(kWriterThreads, 4)
+__global__ void __launch_bounds__(kWriterThreads, kWriterWarpsPerSm * 32 / kWriterThreads)
 mla_kv_write_kernel(uint8_t* __restrict__ cache, int64_t num_slots, int64_t row_bytes,
                     const int64_t* __restrict__ slot_idx,
                     const uint16_t* __restrict__ latent,
@@ -186,16 +187,18 @@ extern "C" int mla_kv_write(mla_kv_cache_t kv, const int64_t* slot_idx, const vo
     int* err = mla_host::device_error_word();
     const int sms = mla_host::sm_count();
     if (err == nullptr || sms <= 0) return MLA_ECUDA;
-    // One row per warp while that takes at most two CTAs per SM (a small batch is
+    // One row per warp while that takes at most 16 warps per SM (a small batch is
     // done soonest by the most warps); above that two rows per warp, both rows'
-    // loads in flight together, and at most four CTAs per SM (32 warps) with the
-    // grid striding over larger batches. Measured with 100 calls per graph: 8,192
-    // rows 4.0 us per call against 5.4 at one row per warp on up to eight CTAs
-    // per SM; 1,048,575 rows 0.85 of the HBM copy rate against 0.75.
+    // loads in flight together, and at most kWriterWarpsPerSm warps per SM with the
+    // grid striding over larger batches. Small CTAs spread the warps evenly over
+    // the SMs. Measured with 100 calls per graph: 8,192 rows 4.0 us per call
+    // against 5.4 at one row per warp on all 64 warp slots; 1,048,575 rows 0.87
+    // of the HBM copy rate against 0.75.
     const int64_t warps_per_cta = kWriterThreads / 32;
+    const int64_t ctas_per_sm = kWriterWarpsPerSm / warps_per_cta;
     int64_t blocks = (n_rows + warps_per_cta - 1) / warps_per_cta;
-    if (blocks > 2 * static_cast<int64_t>(sms)) blocks = (n_rows + 2 * warps_per_cta - 1) / (2 * warps_per_cta);
-    const int64_t max_blocks = static_cast<int64_t>(sms) * 4;
+    if (blocks > static_cast<int64_t>(sms) * ctas_per_sm / 2) blocks = (n_rows + 2 * warps_per_cta - 1) / (2 * warps_per_cta);
+    const int64_t max_blocks = static_cast<int64_t>(sms) * ctas_per_sm;
     if (blocks > max_blocks) blocks = max_blocks;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(blocks));
