@@ -68,15 +68,27 @@ constexpr int kUCtasPerSm = 2;
 // Two products rounded to BF16 by the hardware conversion (round to nearest even
 // of the fp32 product). That is the nearest BF16 of the exact product unless the
 // fp32 product sits on a BF16 midpoint, is NaN, or is nonzero below 2^-100. The
-// last two are ruled out per row (row_needs_exact); a midpoint raises `exact`, and
-// such rows are redone by product_to_bf16.
-__device__ __forceinline__ uint32_t pair_to_bf16x2(float v0, float v1, float s, bool& exact) {
-    const float p0 = __fmul_rn(v0, s), p1 = __fmul_rn(v1, s);
-    const uint32_t u0 = __float_as_uint(p0), u1 = __float_as_uint(p1);
-    exact |= ((u0 & 0xFFFFu) == 0x8000u) | ((u1 & 0xFFFFu) == 0x8000u);
+// last two are ruled out per row (row_needs_exact); midpoints are tracked below,
+// and a row slice with any of them is redone by product_to_bf16.
+// The two products come from one packed fp32 multiply (the same IEEE product per
+// value); their low 16 bits, each XORed with 0x8000, go into a running unsigned
+// 16x2 minimum, which ends with a zero half exactly when some product sat on a
+// BF16 midpoint (midpoint_seen).
+__device__ __forceinline__ uint32_t pair_to_bf16x2(float v0, float v1, uint64_t s2, uint32_t& lows_min) {
+    uint64_t v2, p2;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(v2) : "f"(v0), "f"(v1));
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(p2) : "l"(v2), "l"(s2));
+    float p0, p1;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(p0), "=f"(p1) : "l"(p2));
+    const uint32_t lows = __byte_perm(__float_as_uint(p0), __float_as_uint(p1), 0x5410) ^ 0x80008000u;
+    asm("min.u16x2 %0, %1, %2;" : "=r"(lows_min) : "r"(lows_min), "r"(lows));
     uint32_t r;
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(p1), "f"(p0));   // high half <- p1
     return r;
+}
+
+__device__ __forceinline__ bool midpoint_seen(uint32_t lows_min) {
+    return (lows_min & 0xFFFFu) == 0u || (lows_min >> 16) == 0u;
 }
 
 // Whether a lane's 16 codes with tile scale s can give a product that the
@@ -187,10 +199,12 @@ mla_gather_upconvert_kernel(const uint8_t* __restrict__ cache, int64_t num_slots
                 v[4 * q + 3] = __half2float(__ushort_as_half(static_cast<unsigned short>(h23 >> 16)));
             }
             uint32_t o[8];
-            bool exact = row_needs_exact(codes, sc);
+            uint64_t s2;
+            asm("mov.b64 %0, {%1, %1};" : "=l"(s2) : "f"(sc));
+            uint32_t lows_min = 0xFFFFFFFFu;
 #pragma unroll
-            for (int q = 0; q < 8; ++q) o[q] = pair_to_bf16x2(v[2 * q], v[2 * q + 1], sc, exact);
-            if (exact) {                                              // rare
+            for (int q = 0; q < 8; ++q) o[q] = pair_to_bf16x2(v[2 * q], v[2 * q + 1], s2, lows_min);
+            if (row_needs_exact(codes, sc) || midpoint_seen(lows_min)) {   // rare
 #pragma unroll
                 for (int q = 0; q < 8; ++q)
                     o[q] = product_to_bf16(v[2 * q], sc) | (product_to_bf16(v[2 * q + 1], sc) << 16);
